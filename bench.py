@@ -1,0 +1,473 @@
+"""Benchmark of the paged KV cache hot path on GB300.
+
+One step = one decode step of a Qwen3-0.6B-shaped model over its 28 layers: for each layer,
+kv_store of the 256 sequences' new K/V into that layer's block pool, then paged decode
+attention of the 256 queries over contexts drawn uniform in [100, 2048] (blocks drawn at
+random from a pool sized to 90% of free HBM). Inputs are synthetic and already in HBM when
+the timed region starts; every layer reads 1.13 GB of KV, far more than the 129 MB L2.
+
+The JSON line reports the step's algorithmic HBM bytes per second (value), KV-tokens/s, the
+decode kernel's roofline fraction, the same metric end to end through the public API with
+host buffers (e2e), the varlen-prefill store's GB/s and the prefill TFLOP/s measured in the
+same run, and the CPU oracle timed on the host cores as a baseline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+With N > 1 (torchrun, one process per GPU) every rank runs its own full batch (weak scaling;
+no data-path collective) and rank 0 prints the line; value = bytes of all ranks / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as w  # noqa: E402
+
+METRIC = ("paged decode attn HBM GB/s (% of peak) & KV-tokens/s; kv_store GB/s; "
+          "prefill TFLOP/s")
+LAYERS = w.NUM_LAYERS
+B, HQ, HKV, D, BS = 256, w.NUM_Q_HEADS, w.NUM_KV_HEADS, w.HEAD_DIM, w.BLOCK_SIZE
+ROW_BYTES = HKV * D * 2                     # one token's K (or V) row in one layer
+BLOCK_BYTES_ALL_LAYERS = 2 * LAYERS * BS * ROW_BYTES
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+WORKLOAD = ("qwen3-0.6b decode step: 28 layers x (kv_store of 256 new tokens + paged decode "
+            "attention), B=256, ctx U[100,2048] (seed 2), block_size 256, 16 q / 8 kv heads, "
+            "head_dim 128, bf16 N(0,1), pool [2,28,NB,256,8,128] at 90% of free HBM")
+
+
+# ----------------------------------------------------------------------------- helpers
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        hbm = d.get("hbm_gbs") or d.get("hbm_GBps") or d.get("hbm")
+        bf16 = d.get("bf16_tflops") or d.get("bf16")
+        sus = d.get("bf16_tflops_sustained") or bf16
+        if hbm:
+            return float(hbm), float(bf16 or FALLBACK_BF16_TFLOPS), float(sus or 0), "measured"
+    except (OSError, ValueError, TypeError):
+        pass
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx.append(float(p[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Timing reduction only (no data-path collective): the slowest rank's time."""
+    if world == 1:
+        return x
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def decode_bytes(ctx: np.ndarray, W: int) -> dict:
+    """Algorithmic HBM bytes of one layer: the store and the decode call."""
+    Bn = len(ctx)
+    store = Bn * 2 * ROW_BYTES * 2 + Bn * 8                     # read k,v + write rows + slots
+    decode = (int(ctx.sum()) * 2 * ROW_BYTES + 2 * Bn * HQ * D * 2 + 4 * Bn + 4 * Bn * W)
+    return {"store": store, "decode": decode}
+
+
+# --------------------------------------------------------------------------- decode step
+class DecodeStep:
+    def __init__(self, pkv, seed: int = 2, pool_fraction: float = 0.9, batch: int = B,
+                 num_blocks: int | None = None, rank: int = 0, world: int = 1):
+        self.pkv = pkv
+        free, _ = torch.cuda.mem_get_info()
+        ctx = w.qwen3_decode_lengths(seed, batch, rank=rank, world=world)
+        need = w.blocks_needed(ctx)
+        self.num_blocks = (int(pool_fraction * free // BLOCK_BYTES_ALL_LAYERS)
+                           if num_blocks is None else num_blocks)
+        if self.num_blocks < need:
+            raise RuntimeError(f"pool of {self.num_blocks} blocks < {need} needed")
+        self.lay = w.qwen3_decode_layout(self.num_blocks, seed, batch, rank, world)
+        lay = self.lay
+        self.B = lay.batch
+        self.pool = torch.empty((2, LAYERS, self.num_blocks, BS, HKV, D), dtype=torch.bfloat16,
+                                device="cuda")
+        ids = torch.from_numpy(np.unique(lay.block_tables[lay.block_tables >= 0])).long().cuda()
+        for l in range(LAYERS):      # only referenced blocks hold data (untimed)
+            for kv in range(2):
+                self.pool[kv, l][ids] = w.device_bf16_normal((len(ids), BS, HKV, D),
+                                                             10_000 + 2 * l + kv)
+        self.q = w.device_bf16_normal((LAYERS, self.B, HQ, D), 20_001)
+        self.kn = w.device_bf16_normal((LAYERS, self.B, HKV, D), 20_002)
+        self.vn = w.device_bf16_normal((LAYERS, self.B, HKV, D), 20_003)
+        self.out = torch.empty_like(self.q)
+        self.slots = torch.from_numpy(lay.slot_mapping).cuda()
+        self.tables = torch.from_numpy(lay.block_tables).cuda()
+        self.ctx = torch.from_numpy(lay.context_lens).cuda()
+        self.maxc = lay.max_context_len
+        self.ws = pkv.decode_workspace(self.B, HQ, HKV, D, self.maxc, 0)
+        self.splits_workspace = pkv.decode_workspace_bytes(self.B, HQ, HKV, D, self.maxc, 0)
+        self.bytes = decode_bytes(lay.context_lens, lay.block_tables.shape[1])
+        self.step_bytes = LAYERS * (self.bytes["store"] + self.bytes["decode"])
+        self.kv_tokens = LAYERS * int(lay.context_lens.sum())
+
+    def run(self, events=None):
+        pkv, s = self.pkv, self.pool
+        for l in range(LAYERS):
+            pkv.kv_store(self.kn[l], self.vn[l], self.slots, s[0, l], s[1, l])
+            if events is not None:
+                events.append(torch.cuda.Event(enable_timing=True))
+                events[-1].record()
+            pkv.paged_decode_attn(self.q[l], s[0, l], s[1, l], self.tables, self.ctx, self.maxc,
+                                  self.lay.scale, workspace=self.ws, out=self.out[l])
+            if events is not None:
+                events.append(torch.cuda.Event(enable_timing=True))
+                events[-1].record()
+
+    def launches_per_step(self):
+        return LAYERS * (2 + (1 if self.splits_workspace > 0 else 0))
+
+
+def time_e2e(step: DecodeStep, steps: int):
+    """The same step through the public API with host buffers: every step copies its inputs
+    (q, k, v of 28 layers, slot_mapping, block_tables, context_lens) from pinned host memory
+    and reads the 28 layers' outputs back."""
+    host_in = {n: getattr(step, n).cpu().pin_memory() for n in ("q", "kn", "vn", "slots",
+                                                                "tables", "ctx")}
+    host_out = torch.empty_like(step.out, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        for n, t in host_in.items():
+            getattr(step, n).copy_(t, non_blocking=True)
+        step.run()
+        host_out.copy_(step.out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    dt = (time.perf_counter() - t0) / steps
+    return dt, h2d, d2h
+
+
+def time_prefill_store(pkv, iters: int = 20):
+    """kv_store of the varlen-prefill workload: 256 prompts, lengths U[100, 1024]."""
+    lens = w.varlen_prefill_lengths()
+    lay = w.varlen_prefill_layout(num_blocks=w.blocks_needed(lens) + 64)
+    T = int(lens.sum())
+    k = w.device_bf16_normal((T, HKV, D), 301)
+    v = w.device_bf16_normal((T, HKV, D), 302)
+    kc = torch.empty((lay.num_blocks, BS, HKV, D), dtype=torch.bfloat16, device="cuda")
+    vc = torch.empty_like(kc)
+    slots = torch.from_numpy(lay.slot_mapping).cuda()
+    for _ in range(3):
+        pkv.kv_store(k, v, slots, kc, vc)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(iters):
+        pkv.kv_store(k, v, slots, kc, vc)
+    e1.record()
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / 1e3 / iters
+    nbytes = 2 * T * ROW_BYTES * 2 + 8 * T
+    del k, v, kc, vc
+    return {"tokens": T, "gbs": nbytes / t / 1e9, "us": t * 1e6,
+            "bytes": nbytes, "l2": "inputs (1.18 GB) larger than L2"}
+
+
+def time_prefill(pkv, iters: int = 10):
+    """Varlen causal prefill attention: 256 prompts, lengths U[100, 1024], packed layout;
+    one layer timed (x28 for a model)."""
+    lens = w.varlen_prefill_lengths()
+    cu = torch.from_numpy(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)).cuda()
+    T = int(lens.sum())
+    q = w.device_bf16_normal((T, HQ, D), 401)
+    k = w.device_bf16_normal((T, HKV, D), 402)
+    v = w.device_bf16_normal((T, HKV, D), 403)
+    out = torch.empty_like(q)
+    mx = int(lens.max())
+    try:
+        pkv.varlen_prefill_attn(q, k, v, cu, cu, mx, mx, D ** -0.5, out=out)
+    except pkv.PkvError as e:
+        return {"unavailable": str(e)}
+    for _ in range(2):
+        pkv.varlen_prefill_attn(q, k, v, cu, cu, mx, mx, D ** -0.5, out=out)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(iters):
+        pkv.varlen_prefill_attn(q, k, v, cu, cu, mx, mx, D ** -0.5, out=out)
+    e1.record()
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / 1e3 / iters
+    pairs = int((lens.astype(np.int64) * (lens + 1) // 2).sum())
+    flops = 4 * HQ * D * pairs
+    return {"tflops": flops / t / 1e12, "ms": t * 1e3, "flops": flops, "causal_pairs": pairs}
+
+
+def oracle_decode_sample(step: DecodeStep | None, seqs: int | None, layer: int = 0):
+    """Inputs of one layer for the CPU oracle: referenced blocks copied to a compact host
+    pool (untimed)."""
+    import oracle  # CPU baseline only
+    lay = step.lay
+    rows = np.arange(lay.batch if seqs is None else seqs)
+    tabs = lay.block_tables[rows]
+    ids = np.unique(tabs[tabs >= 0])
+    remap = np.full(lay.num_blocks, -1, np.int64)
+    remap[ids] = np.arange(len(ids))
+    idt = torch.from_numpy(ids).long().cuda()
+
+    def bits(t):
+        return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+    kc = bits(step.pool[0, layer][idt])
+    vc = bits(step.pool[1, layer][idt])
+    bt = np.where(tabs >= 0, remap[np.maximum(tabs, 0)], -1).astype(np.int32)
+    slots_blk = remap[lay.slot_mapping[rows] // BS] * BS + lay.slot_mapping[rows] % BS
+    return dict(oracle=oracle, q=bits(step.q[layer])[rows], kn=bits(step.kn[layer])[rows],
+                vn=bits(step.vn[layer])[rows], kc=kc, vc=vc, bt=bt,
+                ctx=lay.context_lens[rows], slots=slots_blk.astype(np.int64),
+                bytes=decode_bytes(lay.context_lens[rows], lay.block_tables.shape[1]))
+
+
+def oracle_step_time(s) -> float:
+    o = s["oracle"]
+    t0 = time.perf_counter()
+    o.kv_store(s["kn"], s["vn"], s["slots"], s["kc"], s["vc"])
+    o.paged_decode(s["q"], s["kc"], s["vc"], s["bt"], s["ctx"], D ** -0.5)
+    return time.perf_counter() - t0
+
+
+# ------------------------------------------------------------------------------- arms
+def load_pkv():
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "_pkv_build", os.path.join(ROOT, "paged_kv_cache_208_gb300", "build.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod.build()
+    import paged_kv_cache_208_gb300 as pkv
+    return pkv
+
+
+def run_ours(args):
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    pkv = load_pkv()
+    hbm_peak, bf16_peak, bf16_sus, peak_src = peaks()
+
+    step = DecodeStep(pkv, pool_fraction=args.pool_fraction, rank=rank, world=world)
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    if pkv.get_device_errors():
+        raise RuntimeError("device error bits set during warm-up")
+
+    events = []
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        barrier(world)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            step.run(events)
+        e1.record()
+        torch.cuda.synchronize()
+        barrier(world)
+    elapsed = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+    per_step = elapsed / args.steps
+    decode_times = [a.elapsed_time(b) / 1e3 for a, b in zip(events[0::2], events[1::2])]
+    decode_avg = sum(decode_times) / len(decode_times)
+
+    e2e_dt, h2d, d2h = time_e2e(step, min(args.steps, 20))
+    e2e_dt = max_over_ranks(e2e_dt, world)
+
+    extra = {}
+    if not args.skip_extra:
+        extra["kv_store_prefill"] = time_prefill_store(pkv)
+        extra["prefill"] = time_prefill(pkv)
+        if "tflops" in extra["prefill"]:
+            extra["prefill"]["frac_of_bf16_peak"] = extra["prefill"]["tflops"] / bf16_peak
+            extra["prefill"]["tflops_x28_layers_ms"] = extra["prefill"]["ms"] * LAYERS
+
+    cpu = None
+    if rank == 0 and not args.skip_cpu:
+        s = oracle_decode_sample(step, None)
+        import oracle
+        t = oracle_step_time(s)
+        cpu = {"value": (s["bytes"]["store"] + s["bytes"]["decode"]) / t / 1e9, "unit": "GB/s",
+               "cores": oracle.max_threads(), "kind": "oracle",
+               "sample": "one layer (of 28) of the full batch: kv_store + paged decode of all "
+                         "256 sequences, fp64 C oracle with OpenMP",
+               "seconds": t}
+    if rank != 0:
+        return
+    total_bytes = step.step_bytes * world
+    dec_bytes = step.bytes["decode"]
+    achieved = dec_bytes / decode_avg / 1e9
+    line = {
+        "metric": METRIC,
+        "value": total_bytes / per_step / 1e9,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": per_step * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, seeded lengths and block draws)",
+        "config": {"workload": WORKLOAD, "batch": step.B, "layers": LAYERS,
+                   "sum_ctx": int(step.lay.context_lens.sum()), "num_blocks": step.num_blocks,
+                   "pool_gb": round(step.pool.numel() * 2 / 1e9, 1),
+                   "splits": "auto", "l2": "inputs larger than L2 (1.13 GB of KV per layer)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "kv_tokens_per_s": step.kv_tokens * world / per_step,
+        "decode_frac_of_hbm_peak": achieved / hbm_peak,
+        "roofline": {"bound": "hbm", "kernel": "paged_decode_attn (split + combine)",
+                     "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "peak_source": peak_src,
+                     "traffic": None, "algorithmic_bytes_per_launch": dec_bytes,
+                     "avg_launch_us": decode_avg * 1e6},
+        "e2e": {"value": total_bytes / e2e_dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_dt * 1e3},
+        "gpu_launches": step.launches_per_step() * args.steps,
+        "clocks": clocks.summary(),
+        "cpu_baseline": cpu,
+        "extra": extra,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_reference(args):
+    """The CPU oracle timed on the host cores, on the same workload and metric: each step is a
+    bounded sample (16 of the 256 sequences of one layer: store + paged decode)."""
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    torch.cuda.set_device(local)
+    pkv = load_pkv()
+    step = DecodeStep(pkv, num_blocks=w.blocks_needed(w.qwen3_decode_lengths()) + 64)
+    step.run()
+    torch.cuda.synchronize()
+    import oracle
+    s = oracle_decode_sample(step, 16)
+    base_kc, base_vc = s["kc"].copy(), s["vc"].copy()
+    times = []
+    for i in range(args.warmup + args.steps):
+        s["kc"], s["vc"] = base_kc.copy(), base_vc.copy()
+        t = oracle_step_time(s)
+        if i >= args.warmup:
+            times.append(t)
+    per = sum(times) / len(times)
+    nbytes = s["bytes"]["store"] + s["bytes"]["decode"]
+    value = nbytes / per / 1e9
+    sample = ("16 of the 256 sequences of one layer per step: kv_store + paged decode, "
+              "fp64 C oracle with OpenMP")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (same seeded workload)",
+        "config": {"workload": WORKLOAD, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.max_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--pool-fraction", type=float, default=0.9,
+                    help="fraction of free HBM for the KV pool (the workload says 0.9)")
+    ap.add_argument("--skip-extra", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,207 @@
+/*
+ * pkv.h -- C ABI of libpkv, the paged KV cache kernels for GB300 (sm_103a).
+ *
+ * The library implements the data-parallel hot path of the paged KV cache that the nano-vLLM
+ * pages describe («nano-vLLM 最小化vLLM重新实现», 架构 4 模型运行器 and 架构 5 注意力机制):
+ *
+ *   pkv_kv_store             store each new token's K/V into the block pool via slot_mapping
+ *   pkv_paged_decode_attn    one query token per sequence over its paged KV (GQA)
+ *   pkv_varlen_prefill_attn  causal attention over cu_seqlens-packed prompts, keys either
+ *                            packed or read from the pool through a block table
+ *
+ * Common rules
+ *  - Every pointer argument except `stream` is a DEVICE pointer, allocated and owned by the
+ *    caller. The library allocates nothing and frees nothing; it keeps no pointer after a
+ *    call returns.
+ *  - bf16 tensors are passed as `void*` to 16-bit storage. The innermost dimension (head_dim)
+ *    is contiguous; token strides are given in elements where the argument list has one.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream). Every call only enqueues
+ *    work on it: it never synchronises the host, so it may be captured into a CUDA graph.
+ *  - The KV pool of one layer is [num_blocks, block_size, num_kv_heads, head_dim] bf16, i.e.
+ *    one slice of the engine's [2, num_layers, num_blocks, block_size, num_kv_heads,
+ *    head_dim] tensor; K and V pools are separate pointers with the same layout. A "slot" is
+ *    block_id * block_size + offset, a row of the [num_blocks * block_size, num_kv_heads,
+ *    head_dim] view.
+ *  - Errors in scalar arguments are found on the host before anything is enqueued and are
+ *    returned as a status; nothing is written then. Shapes that are valid but that the
+ *    kernels do not implement return PKV_ERR_UNSUPPORTED. A failed launch returns
+ *    PKV_ERR_CUDA. Zero-size work (no tokens, no sequences) returns PKV_OK and enqueues
+ *    nothing.
+ *  - Errors in device DATA (a slot or block id out of range, a context longer than the
+ *    block table row) cannot be seen by the host without a sync. The kernels skip the bad
+ *    access (no out-of-bounds read or write happens) and set a bit in a device-side error
+ *    word, which pkv_get_device_errors() reads.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t pkv_status;
+
+#define PKV_OK 0
+#define PKV_ERR_INVALID_ARG 1 /* null pointer, negative size, Hq % Hkv != 0, bad stride */
+#define PKV_ERR_UNSUPPORTED 2 /* valid but not implemented: head_dim != 128, block_size % 256 */
+#define PKV_ERR_WORKSPACE 3   /* workspace missing or smaller than the query says */
+#define PKV_ERR_CUDA 4        /* a CUDA runtime/driver call failed (launch, tensor map) */
+
+/* bits of the device-side error word */
+#define PKV_DEVERR_SLOT_RANGE 1u      /* kv_store: slot_mapping[t] >= num_slots */
+#define PKV_DEVERR_BLOCK_RANGE 2u     /* attention: block id < 0 or >= num_blocks */
+#define PKV_DEVERR_CONTEXT_RANGE 4u   /* decode: context_lens[b] < 0, > max_context_len,
+                                         or > block_table_width * block_size */
+#define PKV_DEVERR_SEQLEN_RANGE 8u    /* prefill: bad cu_seqlens entry */
+#define PKV_DEVERR_TIMEOUT 16u        /* a pipeline wait gave up (the kernel returned early) */
+
+/* Human-readable name of a status code. Never NULL; the string is static. */
+const char *pkv_status_string(pkv_status status);
+
+/* Version of this ABI (incremented on any incompatible change). */
+int32_t pkv_abi_version(void);
+
+/*
+ * Read the device-side error word of the current device (the OR of the PKV_DEVERR_* bits set
+ * by kernels since the last reset) into *errors, and reset it to 0 when `reset` != 0.
+ * Synchronises the current device first: a diagnostic, not for the hot loop.
+ */
+pkv_status pkv_get_device_errors(uint32_t *errors, int32_t reset);
+
+/*
+ * kv_store -- the Triton store_kvcache of nano-vLLM («nano-vLLM 最小化vLLM重新实现»,
+ * 架构 5: "writes K/V into the paged cache using slot_mapping, no Python loop").
+ *
+ * For every token t in [0, num_tokens) with slot_mapping[t] >= 0:
+ *     k_cache[slot_mapping[t], :, :] = k[t, :, :]
+ *     v_cache[slot_mapping[t], :, :] = v[t, :, :]
+ * A negative slot skips the token (padding). Slots of one call must be unique (a duplicate
+ * leaves one of the two rows, which one is unspecified). A slot >= num_slots is skipped and
+ * sets PKV_DEVERR_SLOT_RANGE.
+ *
+ * k, v:          [num_tokens, num_kv_heads, head_dim] bf16; token t's row starts
+ *                k_tok_stride (v_tok_stride) elements after token t-1's, and a row's
+ *                num_kv_heads * head_dim elements are contiguous (views into a fused qkv
+ *                buffer are fine). Strides must be >= num_kv_heads * head_dim.
+ * slot_mapping:  [num_tokens] int64.
+ * k_cache, v_cache: [num_slots, num_kv_heads, head_dim] bf16 (a per-layer pool,
+ *                num_slots = num_blocks * block_size).
+ * Returns PKV_ERR_INVALID_ARG for null pointers with num_tokens > 0, negative sizes, or
+ * strides shorter than a row. Any head count and head_dim are accepted; rows whose byte
+ * length and addresses are multiples of 16 take the vectorised path.
+ */
+pkv_status pkv_kv_store(const void *k, int64_t k_tok_stride, const void *v, int64_t v_tok_stride,
+                        const int64_t *slot_mapping, int64_t num_tokens, void *k_cache,
+                        void *v_cache, int64_t num_slots, int32_t num_kv_heads,
+                        int32_t head_dim, void *stream);
+
+/*
+ * Bytes of device workspace that pkv_paged_decode_attn needs for these sizes (0 when the
+ * chosen split count is 1). `num_splits` must be the value later passed to the call (0 =
+ * automatic choice, made from the sizes and the current device's SM count). The workspace
+ * holds each split's partial output [batch, num_q_heads, splits, head_dim] fp32 and its
+ * log-sum-exp [batch, num_q_heads, splits] fp32. Returns 0 for invalid sizes.
+ */
+size_t pkv_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t max_context_len,
+                                  int32_t num_splits);
+
+/*
+ * paged_decode_attn -- flash_attn_with_kvcache over the paged cache («nano-vLLM
+ * 最小化vLLM重新实现», 架构 5: decode uses the paged KV cache through block tables and
+ * cache lengths), written as split-K flash-decoding.
+ *
+ * For each sequence b in [0, batch) and query head hq in [0, num_q_heads), with
+ * h = hq / (num_q_heads / num_kv_heads) and L = context_lens[b]:
+ *     key/value i (0 <= i < L) is row  block_tables[b, i / block_size] * block_size
+ *                                       + i % block_size  of k_cache / v_cache, head h
+ *     s_i = scale * dot(q[b, hq, :], k_i)
+ *     out[b, hq, :] = sum_i exp(s_i - max s) v_i / sum_i exp(s_i - max s)    (bf16, RNE)
+ * L = 0 gives zeros. The token stored this step is expected at position L - 1, so the call
+ * comes after pkv_kv_store on the same stream.
+ *
+ * q:             [batch, num_q_heads, head_dim] bf16, contiguous.
+ * k_cache, v_cache: [num_blocks, block_size, num_kv_heads, head_dim] bf16.
+ * block_tables:  [batch, block_table_width] int32; only the first ceil(L / block_size)
+ *                entries of row b are read (padding entries are never dereferenced).
+ * context_lens:  [batch] int32, each <= max_context_len.
+ * num_splits:    0 = automatic; otherwise the number of KV splits for the longest context
+ *                (each split covers the same number of logical tokens, a multiple of 64;
+ *                shorter sequences use fewer splits). Results are identical for any
+ *                physical placement of the blocks; they differ by rounding across values of
+ *                num_splits.
+ * workspace:     pkv_decode_workspace_bytes(...) bytes, 16-byte aligned (may be NULL when
+ *                that is 0). Contents on entry are ignored.
+ * out:           [batch, num_q_heads, head_dim] bf16.
+ * Implemented: head_dim == 128, block_size a multiple of 256 (the pages: block size must be
+ * a multiple of 256), any num_q_heads / num_kv_heads, q, pools and out 16-byte aligned.
+ */
+pkv_status pkv_paged_decode_attn(const void *q, const void *k_cache, const void *v_cache,
+                                 const int32_t *block_tables, int32_t block_table_width,
+                                 const int32_t *context_lens, int32_t batch,
+                                 int32_t max_context_len, int32_t num_q_heads,
+                                 int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                 int64_t num_blocks, float scale, int32_t num_splits,
+                                 void *workspace, size_t workspace_bytes, void *out,
+                                 void *stream);
+
+/*
+ * Bytes of device workspace that pkv_varlen_prefill_attn needs (currently 0 for every
+ * size; the argument pair is kept so that a scheduler state can be added without an ABI
+ * change).
+ */
+size_t pkv_prefill_workspace_bytes(int32_t num_seqs, int32_t max_seqlen_q,
+                                   int32_t num_q_heads, int32_t head_dim);
+
+/*
+ * varlen_prefill_attn -- flash_attn_varlen_func («nano-vLLM 最小化vLLM重新实现», 架构 5:
+ * prefill over variable-length sequences, with an optional block_table for prefix caching).
+ *
+ * Sequence n has Lq = cu_seqlens_q[n+1] - cu_seqlens_q[n] queries and
+ * Lk = cu_seqlens_k[n+1] - cu_seqlens_k[n] keys. For query i of sequence n and query head hq
+ * (KV head h = hq / (num_q_heads / num_kv_heads)):
+ *     visible keys  j <= i + (Lk - Lq)  when causal != 0 (aligned to the end of the keys, so
+ *                   with a cached prefix query i sits at absolute position Lk - Lq + i),
+ *                   all Lk keys otherwise
+ *     out[cu_seqlens_q[n] + i, hq, :] = softmax_j(scale * q . k_j) v_j          (bf16, RNE)
+ * A query that sees no key (Lq > Lk with causal) gets zeros.
+ *
+ * q:             [total_q, num_q_heads, head_dim] bf16, token stride q_tok_stride elements;
+ *                total_q >= cu_seqlens_q[num_seqs] (the rows the tensor really has: tiles
+ *                that reach past them read zeros instead).
+ * k, v:          block_table == NULL: packed [total_k, num_kv_heads, head_dim] bf16, key j of
+ *                sequence n at row cu_seqlens_k[n] + j, token stride kv_tok_stride;
+ *                total_k >= cu_seqlens_k[num_seqs].
+ *                block_table != NULL: the per-layer pools [num_blocks, block_size,
+ *                num_kv_heads, head_dim]; key j of sequence n at row
+ *                block_table[n, j / block_size] * block_size + j % block_size;
+ *                kv_tok_stride must then be num_kv_heads * head_dim; total_k is ignored.
+ *                Pool rows past a sequence's last key are never used: the kernel zeroes
+ *                them in shared memory, so stale or NaN contents do not leak in.
+ * cu_seqlens_q, cu_seqlens_k: [num_seqs + 1] int32, non-decreasing, starting at 0.
+ * max_seqlen_q, max_seqlen_k: upper bounds of Lq and Lk over the batch.
+ * block_table:   NULL, or [num_seqs, block_table_width] int32.
+ * out:           [Tq, num_q_heads, head_dim] bf16, contiguous.
+ * Implemented: head_dim == 128, block_size a multiple of 256 when block_table is given,
+ * num_q_heads / num_kv_heads in {1, 2, 4, 8}, token strides that are multiples of 8 elements, and
+ * 16-byte aligned q, k, v.
+ */
+pkv_status pkv_varlen_prefill_attn(const void *q, int64_t q_tok_stride, int64_t total_q,
+                                   const void *k, const void *v, int64_t kv_tok_stride,
+                                   int64_t total_k,
+                                   const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                                   int32_t num_seqs, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                                   const int32_t *block_table, int32_t block_table_width,
+                                   int32_t block_size, int64_t num_blocks, int32_t num_q_heads,
+                                   int32_t num_kv_heads, int32_t head_dim, float scale,
+                                   int32_t causal, void *workspace, size_t workspace_bytes,
+                                   void *out, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -1,0 +1,195 @@
+"""Paged KV cache kernels for GB300 (sm_103a): a thin Python binding over libpkv's C ABI.
+
+The functions here only marshal arguments: they check dtype, device and layout of torch
+tensors, pass raw device pointers and the current CUDA stream to the ``pkv_*`` entry points
+declared in ``include/pkv.h``, and raise ``PkvError`` on a non-zero status. Every step of
+the computation runs in the CUDA library; there is no other implementation to fall back
+to. Importing this package fails if ``libpkv.so`` has not been built
+(``python paged_kv_cache_208_gb300/build.py`` or ``__graft_entry__.build()``).
+
+PyTorch is used for device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpkv.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA = range(5)
+DEVERR_SLOT_RANGE, DEVERR_BLOCK_RANGE, DEVERR_CONTEXT_RANGE = 1, 2, 4
+DEVERR_SEQLEN_RANGE, DEVERR_TIMEOUT = 8, 16
+
+# symbol -> (restype, argtypes); mirrors include/pkv.h
+_P, _I32, _I64, _F, _SZ = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                           ctypes.c_size_t)
+SIGNATURES = {
+    "pkv_status_string": (ctypes.c_char_p, [_I32]),
+    "pkv_abi_version": (_I32, []),
+    "pkv_get_device_errors": (_I32, [ctypes.POINTER(ctypes.c_uint32), _I32]),
+    "pkv_kv_store": (_I32, [_P, _I64, _P, _I64, _P, _I64, _P, _P, _I64, _I32, _I32, _P]),
+    "pkv_decode_workspace_bytes": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32]),
+    "pkv_paged_decode_attn": (_I32, [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32,
+                                     _I32, _I64, _F, _I32, _P, _SZ, _P, _P]),
+    "pkv_prefill_workspace_bytes": (_SZ, [_I32, _I32, _I32, _I32]),
+    "pkv_varlen_prefill_attn": (_I32, [_P, _I64, _I64, _P, _P, _I64, _I64, _P, _P, _I32, _I32,
+                                       _I32, _P, _I32, _I32, _I64, _I32, _I32, _I32, _F, _I32,
+                                       _P, _SZ, _P, _P]),
+}
+
+
+class PkvError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn}: {_LIB.pkv_status_string(status).decode()} (status {status})")
+        self.status = status
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with "
+                          f"`python {os.path.join(_HERE, 'build.py')}` (needs nvcc)")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_LIB = _load()
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (for callers that want the raw C ABI)."""
+    return _LIB
+
+
+def _check(fn: str, status: int) -> None:
+    if status != OK:
+        raise PkvError(fn, status)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream if hasattr(stream, "cuda_stream") else stream)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype) -> None:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def get_device_errors(reset: bool = True) -> int:
+    """OR of the PKV_DEVERR_* bits kernels set since the last reset (synchronises)."""
+    v = ctypes.c_uint32(0)
+    _check("pkv_get_device_errors", _LIB.pkv_get_device_errors(ctypes.byref(v), int(reset)))
+    return int(v.value)
+
+
+def kv_store(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+             k_cache: torch.Tensor, v_cache: torch.Tensor, stream=None) -> None:
+    """k_cache[slot_mapping[t]] = k[t]; v_cache[slot_mapping[t]] = v[t] (negative slot = skip).
+
+    k, v: [T, Hkv, D] bf16 with dense rows (token stride may be larger, e.g. views into a
+    fused qkv tensor); slot_mapping: [T] int64; caches: [NB, bs, Hkv, D] bf16, contiguous.
+    """
+    for t, n in ((k, "k"), (v, "v"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, torch.bfloat16)
+    _need(slot_mapping, "slot_mapping", torch.int64)
+    hkv, d = k_cache.shape[-2], k_cache.shape[-1]
+    for t, n in ((k, "k"), (v, "v")):
+        if t.dim() != 3 or t.shape[1:] != (hkv, d) or t.stride(2) != 1 or t.stride(1) != d:
+            raise ValueError(f"{n} must be [T, {hkv}, {d}] with dense rows")
+    if not (k_cache.is_contiguous() and v_cache.is_contiguous()):
+        raise ValueError("caches must be contiguous")
+    T = slot_mapping.shape[0]
+    _check("pkv_kv_store", _LIB.pkv_kv_store(
+        _ptr(k), k.stride(0) if T else hkv * d, _ptr(v), v.stride(0) if T else hkv * d,
+        _ptr(slot_mapping.contiguous()), T, _ptr(k_cache), _ptr(v_cache),
+        k_cache.numel() // (hkv * d), hkv, d, _stream(stream)))
+
+
+def decode_workspace_bytes(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                           max_context_len: int, num_splits: int = 0) -> int:
+    return int(_LIB.pkv_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim,
+                                               max_context_len, num_splits))
+
+
+def decode_workspace(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                     max_context_len: int, num_splits: int = 0, device=None) -> torch.Tensor:
+    n = decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, max_context_len,
+                               num_splits)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+
+
+def paged_decode_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                      block_tables: torch.Tensor, context_lens: torch.Tensor,
+                      max_context_len: int, scale: float, num_splits: int = 0,
+                      workspace: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                      stream=None) -> torch.Tensor:
+    """One query token per sequence over its paged KV (GQA). q: [B, Hq, D] bf16;
+    caches [NB, bs, Hkv, D] bf16; block_tables [B, W] int32; context_lens [B] int32."""
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, torch.bfloat16)
+    _need(block_tables, "block_tables", torch.int32)
+    _need(context_lens, "context_lens", torch.int32)
+    if not (q.is_contiguous() and k_cache.is_contiguous() and v_cache.is_contiguous()
+            and block_tables.is_contiguous() and context_lens.is_contiguous()):
+        raise ValueError("q, caches, block_tables and context_lens must be contiguous")
+    B, hq, d = q.shape
+    nb, bs, hkv, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = decode_workspace(B, hq, hkv, d, max_context_len, num_splits, q.device)
+    _check("pkv_paged_decode_attn", _LIB.pkv_paged_decode_attn(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+        _ptr(context_lens), B, int(max_context_len), hq, hkv, d, bs, nb, float(scale),
+        int(num_splits), _ptr(workspace), workspace.numel(), _ptr(out), _stream(stream)))
+    return out
+
+
+def varlen_prefill_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                        cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor,
+                        max_seqlen_q: int, max_seqlen_k: int, scale: float, causal: bool = True,
+                        block_table: torch.Tensor | None = None,
+                        out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Causal attention over cu_seqlens-packed sequences. q: [Tq, Hq, D]; k, v: packed
+    [Tk, Hkv, D], or the pools [NB, bs, Hkv, D] when block_table [N, W] int32 is given."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16)
+    _need(cu_seqlens_q, "cu_seqlens_q", torch.int32)
+    _need(cu_seqlens_k, "cu_seqlens_k", torch.int32)
+    tq, hq, d = q.shape
+    if q.stride(2) != 1 or q.stride(1) != d:
+        raise ValueError("q must have dense rows")
+    if block_table is not None:
+        _need(block_table, "block_table", torch.int32)
+        nb, bs, hkv, _ = k.shape
+        if not (k.is_contiguous() and v.is_contiguous() and block_table.is_contiguous()):
+            raise ValueError("pools and block_table must be contiguous")
+        kv_stride, total_k, W = hkv * d, 0, block_table.shape[1]
+    else:
+        total_k, hkv, _ = k.shape
+        if k.stride() != v.stride() or k.stride(2) != 1 or k.stride(1) != d:
+            raise ValueError("k and v must share a layout with dense rows")
+        kv_stride, nb, bs, W = k.stride(0), 0, 0, 0
+    if out is None:
+        out = torch.empty((tq, hq, d), dtype=q.dtype, device=q.device)
+    n = cu_seqlens_q.shape[0] - 1
+    _check("pkv_varlen_prefill_attn", _LIB.pkv_varlen_prefill_attn(
+        _ptr(q), q.stride(0), tq, _ptr(k), _ptr(v), kv_stride, total_k,
+        _ptr(cu_seqlens_q.contiguous()), _ptr(cu_seqlens_k.contiguous()), n, int(max_seqlen_q),
+        int(max_seqlen_k), _ptr(block_table), W, bs, nb, hq, hkv, d, float(scale),
+        int(bool(causal)), None, 0, _ptr(out), _stream(stream)))
+    return out

@@ -1,0 +1,440 @@
+// decode.cu -- paged decode attention as split-K flash-decoding (sm_103a).
+//
+// flash_attn_with_kvcache over the paged cache («nano-vLLM 最小化vLLM重新实现», 架构 5):
+// one query token per sequence attends over its context, whose K/V rows are gathered
+// through the sequence's block table. GQA: query head hq reads KV head hq / G.
+//
+// Work unit (one CTA): sequence b, KV head h, up to two of the G query heads of h (so a
+// CTA reads each K/V byte once for both heads of a Qwen3 group), and one split: the
+// logical tokens [s * chunk, min((s + 1) * chunk, ctx_b)). chunk is a multiple of the 64-
+// token tile and the block size is a multiple of 256, so a tile never straddles a block.
+//
+// Pipeline (per CTA, 8 consumer warps + 1 producer warp):
+//   producer  -- one thread looks up block_tables[b][pos / block_size] and issues two TMA
+//                tensor loads per tile (K and V: 64 tokens x 256 bytes of head h each,
+//                128-byte swizzled) into a 3-stage ring guarded by full/empty mbarriers;
+//   consumers -- warp w owns tokens [8w, 8w + 8) of every tile and keeps its own online-
+//                softmax state (running max m, sum l, accumulator acc) in registers:
+//                  QK:  4 lanes per token, 32 dims per lane, reduced with 2 shuffles;
+//                  PV:  16 lanes per token (8 dims each), two tokens per instruction;
+//                at the end the 8 warp states are merged through shared memory.
+// With one split the CTA writes bf16 output directly; otherwise it writes its normalised
+// partial output and log2-sum-exp, and decode_combine_kernel merges the splits.
+//
+// Algorithmic HBM bytes per (sequence, KV head, token): 256 (K) + 256 (V).
+#include <math.h>
+
+#include <algorithm>
+
+#include "device_common.cuh"
+#include "launch.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kTile = 64;
+constexpr int kConsumerWarps = 8;
+constexpr int kStages = 3;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kTileBytes = kTile * kD * 2;  // one head's K (or V) for 64 tokens: 16 KiB
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr unsigned kFull = 0xffffffffu;
+
+template <int GC>
+struct DecodeSmem {
+  uint8_t k[kStages][kTileBytes];  // must start 1024-byte aligned (128-byte swizzle atoms)
+  uint8_t v[kStages][kTileBytes];
+  float acc[kConsumerWarps][GC][kD];
+  float m[kConsumerWarps][GC];
+  float l[kConsumerWarps][GC];
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+};
+
+// Byte offset of 16-byte chunk j (dims 8j..8j+7) of token t inside a swizzled tile. The TMA
+// box is {64 dims, 2 halves, 64 tokens}: 128-byte row r = 2t + (j >= 8), and the 128-byte
+// swizzle XORs the chunk index within the row with r mod 8.
+__device__ __forceinline__ uint32_t tile_offset(int t, int j) {
+  const int r = 2 * t + (j >> 3);
+  return (uint32_t)((r << 7) | (((j & 7) ^ (r & 7)) << 4));
+}
+
+template <int GC>
+// 112 registers: two 288-thread CTAs (104 KiB of shared memory each) fit on one SM.
+__global__ void __maxnreg__(112)
+    decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap vmap, const uint16_t *__restrict__ q,
+                        const int32_t *__restrict__ block_tables, int32_t table_width,
+                        const int32_t *__restrict__ context_lens, int32_t num_q_heads,
+                        int32_t group, int32_t head_groups, int32_t block_size,
+                        int64_t num_blocks, int32_t chunk, int32_t splits, float qscale,
+                        float *__restrict__ part_o, float *__restrict__ part_lse,
+                        uint16_t *__restrict__ out, unsigned int *err) {
+  const int xg = blockIdx.x;
+  const int h = xg / head_groups;
+  const int hq0 = h * group + (xg % head_groups) * GC;
+  const int s = blockIdx.y;
+  const int b = blockIdx.z;
+
+  // context length, clamped to what the table row and the split grid can address
+  const int64_t cap64 = min((int64_t)table_width * block_size, (int64_t)splits * chunk);
+  int64_t L = context_lens[b];
+  if (L < 0 || L > cap64) {
+    if (s == 0 && xg == 0 && threadIdx.x == 0) record_error(err, 4u /* CONTEXT_RANGE */);
+    L = L < 0 ? 0 : cap64;
+  }
+  const int tok_begin = s * chunk;
+  if (tok_begin >= L) {
+    if (L == 0 && splits == 1 && threadIdx.x < GC * kD) {  // empty context: zeros
+      const int g = threadIdx.x / kD, d = threadIdx.x % kD;
+      out[((int64_t)b * num_q_heads + hq0 + g) * kD + d] = 0;
+    }
+    return;
+  }
+  const int tok_end = (int)min(L, (int64_t)tok_begin + chunk);
+  const int ntiles = (tok_end - tok_begin + kTile - 1) / kTile;
+
+  extern __shared__ uint8_t smem_raw[];
+  DecodeSmem<GC> &sm = *reinterpret_cast<DecodeSmem<GC> *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&sm.full[i], 1);
+      mbar_init(&sm.empty[i], kConsumerWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------------ producer
+    if (lane != 0) return;
+    prefetch_tensormap(&kmap);
+    prefetch_tensormap(&vmap);
+    const uint64_t policy = policy_evict_first();
+    const int32_t *table = block_tables + (int64_t)b * table_width;
+    int issued = 0;
+    for (int it = 0; it < ntiles; ++it) {
+      const int stage = it % kStages;
+      if (it >= kStages && !wait_parity(&sm.empty[stage], ((it / kStages) - 1) & 1)) {
+        record_error(err, 16u /* TIMEOUT */);
+        break;
+      }
+      const int pos = tok_begin + it * kTile;
+      const int64_t blk = table[pos / block_size];
+      int32_t row;
+      if (blk < 0 || blk >= num_blocks) {
+        record_error(err, 2u /* BLOCK_RANGE */);
+        row = -2 * kTile;  // wholly outside the pool: TMA fills zeros, nothing is read
+      } else {
+        row = (int32_t)(blk * block_size + pos % block_size);
+      }
+      mbar_arrive_expect_tx(&sm.full[stage], 2 * kTileBytes);
+      tma_load_3d(sm.k[stage], &kmap, &sm.full[stage], 0, 2 * h, row, policy);
+      tma_load_3d(sm.v[stage], &vmap, &sm.full[stage], 0, 2 * h, row, policy);
+      ++issued;
+    }
+    // keep the CTA alive until every copy it issued has landed
+    for (int it = max(0, issued - kStages); it < issued; ++it)
+      if (!wait_parity(&sm.full[it % kStages], (it / kStages) & 1)) {
+        record_error(err, 16u);
+        break;
+      }
+    return;
+  }
+
+  // -------------------------------------------------------------------- consumers
+  const int tq = lane >> 2;   // QK: token within the warp's 8
+  const int qc = lane & 3;    // QK: quarter -> chunks qc, qc+4, qc+8, qc+12
+  const int hw = lane >> 4;   // PV: token parity
+  const int dl = lane & 15;   // PV: chunk (dims 8dl..8dl+7)
+
+  float qr[GC][4][8];
+#pragma unroll
+  for (int g = 0; g < GC; ++g) {
+    const uint4 *qrow = reinterpret_cast<const uint4 *>(q + ((int64_t)b * num_q_heads + hq0 + g) * kD);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const uint4 w4 = __ldg(qrow + qc + 4 * r);
+      const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        qr[g][r][2 * e] = bf16_lo(w[e]) * qscale;
+        qr[g][r][2 * e + 1] = bf16_hi(w[e]) * qscale;
+      }
+    }
+  }
+
+  float m_run[GC], l_run[GC], acc[GC][8];
+#pragma unroll
+  for (int g = 0; g < GC; ++g) {
+    m_run[g] = -INFINITY;
+    l_run[g] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[g][e] = 0.f;
+  }
+
+  for (int it = 0; it < ntiles; ++it) {
+    const int stage = it % kStages;
+    if (!wait_parity(&sm.full[stage], (it / kStages) & 1)) {
+      if (lane == 0) record_error(err, 16u);
+      break;
+    }
+    const uint8_t *kt = sm.k[stage];
+    const uint8_t *vt = sm.v[stage];
+    const int tile_pos = tok_begin + it * kTile;
+    const int n_valid = tok_end - tile_pos;  // tokens of this tile inside the split (>= 1)
+
+    // ---- scores for token t = 8 warp + tq (log2 domain: q carries scale * log2 e)
+    const int t = warp * 8 + tq;
+    float sc[GC];
+#pragma unroll
+    for (int g = 0; g < GC; ++g) sc[g] = 0.f;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const uint4 k4 = *reinterpret_cast<const uint4 *>(kt + tile_offset(t, qc + 4 * r));
+      const uint32_t w[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float k0 = bf16_lo(w[e]), k1 = bf16_hi(w[e]);
+#pragma unroll
+        for (int g = 0; g < GC; ++g) {
+          sc[g] = fmaf(qr[g][r][2 * e], k0, sc[g]);
+          sc[g] = fmaf(qr[g][r][2 * e + 1], k1, sc[g]);
+        }
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < GC; ++g) {
+      sc[g] += __shfl_xor_sync(kFull, sc[g], 1);
+      sc[g] += __shfl_xor_sync(kFull, sc[g], 2);
+      if (t >= n_valid) sc[g] = -INFINITY;
+    }
+
+    // ---- online softmax over the warp's 8 tokens
+    float p[GC];
+    bool any = false;
+#pragma unroll
+    for (int g = 0; g < GC; ++g) {
+      float mx = sc[g];
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+      const float m_new = fmaxf(m_run[g], mx);
+      if (m_new != -INFINITY) {
+        any = true;
+        const float alpha = fast_exp2(m_run[g] - m_new);
+        p[g] = fast_exp2(sc[g] - m_new);
+        float ps = p[g];
+        ps += __shfl_xor_sync(kFull, ps, 4);
+        ps += __shfl_xor_sync(kFull, ps, 8);
+        ps += __shfl_xor_sync(kFull, ps, 16);
+        l_run[g] = l_run[g] * alpha + ps;
+        m_run[g] = m_new;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[g][e] *= alpha;
+      } else {
+        p[g] = 0.f;
+      }
+    }
+
+    // ---- acc += p v, two tokens per instruction (half-warp hw takes token 2i + hw)
+    if (any) {
+      const bool full_tile = n_valid >= kTile;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int tt = 2 * i + hw;
+        float pv[GC];
+#pragma unroll
+        for (int g = 0; g < GC; ++g) pv[g] = __shfl_sync(kFull, p[g], 4 * tt);
+        const int t2 = warp * 8 + tt;
+        if (full_tile || t2 < n_valid) {
+          const uint4 v4 = *reinterpret_cast<const uint4 *>(vt + tile_offset(t2, dl));
+          const uint32_t w[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float v0 = bf16_lo(w[e]), v1 = bf16_hi(w[e]);
+#pragma unroll
+            for (int g = 0; g < GC; ++g) {
+              acc[g][2 * e] = fmaf(pv[g], v0, acc[g][2 * e]);
+              acc[g][2 * e + 1] = fmaf(pv[g], v1, acc[g][2 * e + 1]);
+            }
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[stage]);
+  }
+
+  // ---- merge: half-warps, then the 8 warps through shared memory
+#pragma unroll
+  for (int g = 0; g < GC; ++g)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[g][e] += __shfl_xor_sync(kFull, acc[g][e], 16);
+  if (lane < 16) {
+#pragma unroll
+    for (int g = 0; g < GC; ++g)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sm.acc[warp][g][8 * dl + e] = acc[g][e];
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int g = 0; g < GC; ++g) {
+      sm.m[warp][g] = m_run[g];
+      sm.l[warp][g] = l_run[g];
+    }
+  }
+  named_barrier_sync(1, kConsumerWarps * 32);
+
+  const int g = threadIdx.x / kD;
+  const int d = threadIdx.x % kD;
+  if (g < GC) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm.m[w][g]);
+    float o = 0.f, lse = -INFINITY;
+    if (M != -INFINITY) {
+      float lsum = 0.f, osum = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float f = fast_exp2(sm.m[w][g] - M);
+        lsum = fmaf(sm.l[w][g], f, lsum);
+        osum = fmaf(sm.acc[w][g][d], f, osum);
+      }
+      o = osum / lsum;
+      lse = M + log2f(lsum);
+    }
+    const int64_t row = (int64_t)b * num_q_heads + hq0 + g;
+    if (splits == 1) {
+      out[row * kD + d] = bf16_bits_rn(o);
+    } else {
+      part_o[(row * splits + s) * kD + d] = o;
+      if (d == 0) part_lse[row * splits + s] = lse;
+    }
+  }
+}
+
+// One warp per (sequence, query head): out = sum_s 2^(lse_s - lse) o_s over the sequence's
+// splits, lse = log2 sum_s 2^lse_s. A sequence with no token gets zeros.
+__global__ void __launch_bounds__(128)
+    decode_combine_kernel(const float *__restrict__ part_o, const float *__restrict__ part_lse,
+                          const int32_t *__restrict__ context_lens, int32_t batch,
+                          int32_t num_q_heads, int32_t chunk, int32_t splits, int64_t cap,
+                          uint16_t *__restrict__ out) {
+  const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
+  if (row >= (int64_t)batch * num_q_heads) return;
+  const int lane = threadIdx.x & 31;
+  const int b = (int)(row / num_q_heads);
+  int64_t L = context_lens[b];
+  L = L < 0 ? 0 : (L > cap ? cap : L);
+  const int ns = (int)((L + chunk - 1) / chunk);
+  const float *lse = part_lse + row * splits;
+  float M = -INFINITY;
+  for (int s = lane; s < ns; s += 32) M = fmaxf(M, lse[s]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float wsum = 0.f;
+  if (M != -INFINITY) {
+    for (int s = 0; s < ns; ++s) {
+      const float wgt = fast_exp2(lse[s] - M);
+      const float4 o4 = *reinterpret_cast<const float4 *>(part_o + (row * splits + s) * kD + 4 * lane);
+      wsum += wgt;
+      acc.x = fmaf(wgt, o4.x, acc.x);
+      acc.y = fmaf(wgt, o4.y, acc.y);
+      acc.z = fmaf(wgt, o4.z, acc.z);
+      acc.w = fmaf(wgt, o4.w, acc.w);
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  const uint32_t lo = (uint32_t)bf16_bits_rn(acc.x * inv) | ((uint32_t)bf16_bits_rn(acc.y * inv) << 16);
+  const uint32_t hi = (uint32_t)bf16_bits_rn(acc.z * inv) | ((uint32_t)bf16_bits_rn(acc.w * inv) << 16);
+  *reinterpret_cast<uint2 *>(out + row * kD + 4 * lane) = make_uint2(lo, hi);
+}
+
+template <int GC>
+cudaError_t launch_split(const DecodeArgs &a, const DecodePlan &p, const CUtensorMap &km,
+                         const CUtensorMap &vm, float *part_o, float *part_lse,
+                         cudaStream_t stream) {
+  const size_t smem = sizeof(DecodeSmem<GC>) + 1024;
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<GC>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  const dim3 grid(a.num_kv_heads * p.head_groups, p.splits, a.batch);
+  const int group = a.num_q_heads / a.num_kv_heads;
+  decode_split_kernel<GC><<<grid, kThreads, smem, stream>>>(
+      km, vm, static_cast<const uint16_t *>(a.q), a.block_tables, a.table_width, a.context_lens,
+      a.num_q_heads, group, p.head_groups, a.block_size, a.num_blocks, p.chunk, p.splits,
+      a.scale * kLog2e, part_o, part_lse, static_cast<uint16_t *>(a.out), a.err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                       int32_t max_context_len, int32_t num_splits, int num_sms) {
+  DecodePlan p{};
+  const int group = num_q_heads / num_kv_heads;
+  p.heads_per_cta = (group % 2 == 0) ? 2 : 1;
+  p.head_groups = group / p.heads_per_cta;
+  const int64_t max_ctx = max_context_len > 0 ? max_context_len : 1;
+  const int64_t max_tiles = (max_ctx + kTile - 1) / kTile;
+  if (num_splits > 0) {
+    const int64_t S = num_splits < max_tiles ? num_splits : max_tiles;
+    const int64_t per = (max_ctx + S - 1) / S;
+    p.chunk = (int32_t)((per + kTile - 1) / kTile * kTile);
+  } else {
+    // Smallest chunk (down to one tile) that still gives >= 8 CTAs per SM, capped at 4 tiles
+    // so that long and short contexts balance across the machine.
+    const int64_t units = (int64_t)batch * num_kv_heads * p.head_groups;
+    const int64_t target = (int64_t)num_sms * 8;
+    int64_t chunk = 4 * kTile;
+    while (chunk > kTile && units * ((max_ctx + chunk - 1) / chunk) < target) chunk -= kTile;
+    p.chunk = (int32_t)chunk;
+  }
+  p.splits = (int32_t)((max_ctx + p.chunk - 1) / p.chunk);
+  p.workspace_bytes =
+      p.splits > 1 ? (size_t)batch * num_q_heads * p.splits * (kD + 1) * sizeof(float) : 0;
+  return p;
+}
+
+cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &p, cudaStream_t stream) {
+  // TMA views of the two pools: {64 dims, 2 * Hkv half-heads, num_blocks * block_size rows}
+  CUtensorMap km, vm;
+  const uint64_t rows = (uint64_t)a.num_blocks * a.block_size;
+  const uint64_t dims[3] = {64, (uint64_t)a.num_kv_heads * 2, rows};
+  const uint64_t strides[2] = {128, (uint64_t)a.num_kv_heads * kD * 2};
+  const uint32_t box[3] = {64, 2, kTile};
+  if (encode_tensor_map(&km, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(a.k_cache),
+                        dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B) != CUDA_SUCCESS ||
+      encode_tensor_map(&vm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(a.v_cache),
+                        dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+
+  float *part_o = static_cast<float *>(a.workspace);
+  float *part_lse = part_o ? part_o + (size_t)a.batch * a.num_q_heads * p.splits * kD : nullptr;
+  cudaError_t e = p.heads_per_cta == 2 ? launch_split<2>(a, p, km, vm, part_o, part_lse, stream)
+                                       : launch_split<1>(a, p, km, vm, part_o, part_lse, stream);
+  if (e != cudaSuccess || p.splits == 1) return e;
+  const int64_t rows_out = (int64_t)a.batch * a.num_q_heads;
+  const int64_t cap = std::min((int64_t)a.table_width * a.block_size, (int64_t)p.splits * p.chunk);
+  decode_combine_kernel<<<(unsigned)((rows_out + 3) / 4), 128, 0, stream>>>(
+      part_o, part_lse, a.context_lens, a.batch, a.num_q_heads, p.chunk, p.splits, cap,
+      static_cast<uint16_t *>(a.out));
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,147 @@
+// kv_store.cu -- scatter each new token's K and V rows into the paged pool via slot_mapping.
+//
+// The store of «nano-vLLM 最小化vLLM重新实现», 架构 5 (store_kvcache: K/V written into the
+// paged cache through slot_mapping). One warp moves one token: its K row and its V row
+// (num_kv_heads * head_dim bf16 each; 2 KiB for Qwen3's 8 x 128), as 16-byte vectors, so a
+// warp instruction moves 512 contiguous bytes. All of a lane's loads are issued before its
+// stores. Loads bypass L1 (each byte is read once); stores are ordinary write-back so the
+// rows stay in L2 for the attention kernel that reads them next.
+//
+// HBM traffic per token: 2 rows read + 2 rows written + 8 bytes of slot (algorithmic minimum).
+#include "device_common.cuh"
+#include "launch.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kWarpsPerCta = 8;
+
+// Rows of exactly VEC 16-byte vectors per lane (row = 32 * VEC vectors): fully unrolled.
+template <int VEC>
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+    kv_store_rows_kernel(const uint4 *__restrict__ k, int64_t k_stride, const uint4 *__restrict__ v,
+                         int64_t v_stride, const int64_t *__restrict__ slot_mapping,
+                         int64_t num_tokens, uint4 *__restrict__ k_cache,
+                         uint4 *__restrict__ v_cache, int64_t num_slots, unsigned int *err) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerCta;
+  constexpr int64_t kRow = 32 * VEC;  // vectors per row
+  for (int64_t t = warp0; t < num_tokens; t += nwarps) {
+    const int64_t slot = __ldg(slot_mapping + t);
+    uint4 kr[VEC], vr[VEC];
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+      kr[i] = ld_stream_u4(k + t * k_stride + i * 32 + lane);
+      vr[i] = ld_stream_u4(v + t * v_stride + i * 32 + lane);
+    }
+    if (slot < 0) continue;
+    if (slot >= num_slots) {
+      if (lane == 0) record_error(err, 1u /* PKV_DEVERR_SLOT_RANGE */);
+      continue;
+    }
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+      k_cache[slot * kRow + i * 32 + lane] = kr[i];
+      v_cache[slot * kRow + i * 32 + lane] = vr[i];
+    }
+  }
+}
+
+// Any row length that is a whole number of 16-byte vectors.
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+    kv_store_vec_kernel(const uint4 *__restrict__ k, int64_t k_stride, const uint4 *__restrict__ v,
+                        int64_t v_stride, const int64_t *__restrict__ slot_mapping,
+                        int64_t num_tokens, uint4 *__restrict__ k_cache,
+                        uint4 *__restrict__ v_cache, int64_t num_slots, int64_t row,
+                        unsigned int *err) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerCta;
+  for (int64_t t = warp0; t < num_tokens; t += nwarps) {
+    const int64_t slot = __ldg(slot_mapping + t);
+    if (slot < 0) continue;
+    if (slot >= num_slots) {
+      if (lane == 0) record_error(err, 1u);
+      continue;
+    }
+    for (int64_t i = lane; i < row; i += 32) {
+      k_cache[slot * row + i] = ld_stream_u4(k + t * k_stride + i);
+      v_cache[slot * row + i] = ld_stream_u4(v + t * v_stride + i);
+    }
+  }
+}
+
+// Fallback for rows or addresses that are not 16-byte multiples: one bf16 at a time.
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+    kv_store_u16_kernel(const uint16_t *__restrict__ k, int64_t k_stride,
+                        const uint16_t *__restrict__ v, int64_t v_stride,
+                        const int64_t *__restrict__ slot_mapping, int64_t num_tokens,
+                        uint16_t *__restrict__ k_cache, uint16_t *__restrict__ v_cache,
+                        int64_t num_slots, int64_t row, unsigned int *err) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerCta;
+  for (int64_t t = warp0; t < num_tokens; t += nwarps) {
+    const int64_t slot = __ldg(slot_mapping + t);
+    if (slot < 0) continue;
+    if (slot >= num_slots) {
+      if (lane == 0) record_error(err, 1u);
+      continue;
+    }
+    for (int64_t i = lane; i < row; i += 32) {
+      k_cache[slot * row + i] = k[t * k_stride + i];
+      v_cache[slot * row + i] = v[t * v_stride + i];
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_kv_store(const void *k, int64_t k_tok_stride, const void *v,
+                            int64_t v_tok_stride, const int64_t *slot_mapping, int64_t num_tokens,
+                            void *k_cache, void *v_cache, int64_t num_slots, int64_t row_elems,
+                            unsigned int *err, int num_sms, cudaStream_t stream) {
+  const int64_t warps_needed = num_tokens;
+  const int64_t max_ctas = (int64_t)num_sms * 8;  // 8 CTAs x 8 warps = 64 warps per SM
+  const int64_t ctas64 = (warps_needed + kWarpsPerCta - 1) / kWarpsPerCta;
+  const unsigned int ctas = (unsigned int)(ctas64 < max_ctas ? ctas64 : max_ctas);
+  const dim3 block(kWarpsPerCta * 32);
+
+  auto aligned16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  const bool vec_ok = (row_elems % 8 == 0) && (k_tok_stride % 8 == 0) && (v_tok_stride % 8 == 0) &&
+                      aligned16(k) && aligned16(v) && aligned16(k_cache) && aligned16(v_cache);
+  if (vec_ok) {
+    const int64_t row_v = row_elems / 8;
+    const uint4 *k4 = static_cast<const uint4 *>(k);
+    const uint4 *v4 = static_cast<const uint4 *>(v);
+    uint4 *kc4 = static_cast<uint4 *>(k_cache);
+    uint4 *vc4 = static_cast<uint4 *>(v_cache);
+    const int64_t ks = k_tok_stride / 8, vs = v_tok_stride / 8;
+    switch (row_v) {
+      case 128:  // 8 heads x 128 dims: the Qwen3 row
+        kv_store_rows_kernel<4><<<ctas, block, 0, stream>>>(k4, ks, v4, vs, slot_mapping,
+                                                            num_tokens, kc4, vc4, num_slots, err);
+        break;
+      case 64:
+        kv_store_rows_kernel<2><<<ctas, block, 0, stream>>>(k4, ks, v4, vs, slot_mapping,
+                                                            num_tokens, kc4, vc4, num_slots, err);
+        break;
+      case 256:
+        kv_store_rows_kernel<8><<<ctas, block, 0, stream>>>(k4, ks, v4, vs, slot_mapping,
+                                                            num_tokens, kc4, vc4, num_slots, err);
+        break;
+      default:
+        kv_store_vec_kernel<<<ctas, block, 0, stream>>>(k4, ks, v4, vs, slot_mapping, num_tokens,
+                                                        kc4, vc4, num_slots, row_v, err);
+    }
+  } else {
+    kv_store_u16_kernel<<<ctas, block, 0, stream>>>(
+        static_cast<const uint16_t *>(k), k_tok_stride, static_cast<const uint16_t *>(v),
+        v_tok_stride, slot_mapping, num_tokens, static_cast<uint16_t *>(k_cache),
+        static_cast<uint16_t *>(v_cache), num_slots, row_elems, err);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

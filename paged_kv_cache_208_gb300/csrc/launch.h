@@ -1,0 +1,85 @@
+// launch.h -- host-side launchers behind the C ABI (internal to libpkv).
+//
+// The extern "C" entry points in pkv_api.cu validate arguments and then call these; each
+// launcher only enqueues kernels on `stream` and returns the launch status.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pkv {
+
+// kv_store.cu
+cudaError_t launch_kv_store(const void *k, int64_t k_tok_stride, const void *v,
+                            int64_t v_tok_stride, const int64_t *slot_mapping, int64_t num_tokens,
+                            void *k_cache, void *v_cache, int64_t num_slots, int64_t row_elems,
+                            unsigned int *err, int num_sms, cudaStream_t stream);
+
+// decode.cu
+struct DecodePlan {
+  int32_t chunk;       // logical tokens per split (multiple of 64)
+  int32_t splits;      // splits of the longest context
+  int32_t head_groups; // CTAs per KV head (query heads handled two at a time)
+  int32_t heads_per_cta;
+  size_t workspace_bytes;
+};
+DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                       int32_t max_context_len, int32_t num_splits, int num_sms);
+
+struct DecodeArgs {
+  const void *q;
+  const void *k_cache;
+  const void *v_cache;
+  const int32_t *block_tables;
+  int32_t table_width;
+  const int32_t *context_lens;
+  int32_t batch;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t block_size;
+  int64_t num_blocks;
+  float scale;
+  void *workspace;
+  void *out;
+  unsigned int *err;
+};
+cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &plan,
+                                cudaStream_t stream);
+
+// prefill.cu
+struct PrefillArgs {
+  const void *q;
+  int64_t q_tok_stride;
+  int64_t total_q;   // rows of q (and of out)
+  const void *k;
+  const void *v;
+  int64_t kv_tok_stride;
+  int64_t kv_rows;   // rows addressable through k/v (Tk, or num_blocks * block_size)
+  const int32_t *cu_seqlens_q;
+  const int32_t *cu_seqlens_k;
+  int32_t num_seqs;
+  int32_t max_seqlen_q;
+  int32_t max_seqlen_k;
+  const int32_t *block_table;
+  int32_t table_width;
+  int32_t block_size;
+  int64_t num_blocks;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  float scale;
+  int32_t causal;
+  void *out;
+  unsigned int *err;
+};
+cudaError_t launch_varlen_prefill(const PrefillArgs &a, int num_sms, cudaStream_t stream);
+bool prefill_group_supported(int group);  // num_q_heads / num_kv_heads
+
+// tensor maps (pkv_api.cu): the driver's cuTensorMapEncodeTiled, fetched at run time
+CUresult encode_tensor_map(CUtensorMap *map, CUtensorMapDataType dtype, uint32_t rank,
+                           void *base, const uint64_t *dims, const uint64_t *strides_bytes,
+                           const uint32_t *box, CUtensorMapSwizzle swizzle,
+                           CUtensorMapL2promotion promotion);
+
+}  // namespace pkv

@@ -208,6 +208,25 @@ def decode_values(lay: DecodeLayout, g: np.random.Generator) -> DecodeValues:
     return DecodeValues(q, k_new, v_new, kc, vc, lk, lv)
 
 
+def decode_values_keyed(lay: DecodeLayout, seq_ids, base_seed: int) -> DecodeValues:
+    """Like decode_values, but sequence i's numbers come from their own generator seeded with
+    base_seed + seq_ids[i], so a sequence draws the same values whichever shard holds it."""
+    B, Hq, Hkv, D, bs = lay.batch, lay.num_q_heads, lay.num_kv_heads, lay.head_dim, lay.block_size
+    kc = np.full((lay.num_blocks, bs, Hkv, D), BF16_NAN_CANARY, dtype=np.uint16)
+    vc = np.full_like(kc, BF16_NAN_CANARY)
+    q, lk, lv = [], [], []
+    for b in range(B):
+        g = rng(base_seed + int(seq_ids[b]))
+        L = int(lay.context_lens[b])
+        q.append(host_bf16_normal(g, (Hq, D)))
+        lk.append(host_bf16_normal(g, (L, Hkv, D)))
+        lv.append(host_bf16_normal(g, (L, Hkv, D)))
+        _fill_blocks(kc, lay.block_tables[b], lk[-1][:max(L - 1, 0)], bs)
+        _fill_blocks(vc, lay.block_tables[b], lv[-1][:max(L - 1, 0)], bs)
+    return DecodeValues(np.stack(q), np.stack([x[-1] for x in lk]), np.stack([x[-1] for x in lv]),
+                        kc, vc, lk, lv)
+
+
 def tiny_decode(seed: int = 1):
     """Tiny decode step: 4 sequences, contexts {1, 17, 255, 300}, a pool of 8 blocks handed
     out in a seeded random permutation (1, 1, 1 and 2 blocks)."""
@@ -216,15 +235,28 @@ def tiny_decode(seed: int = 1):
     return lay, decode_values(lay, g)
 
 
-def qwen3_decode_lengths(seed: int = 2, batch: int = 256, lo: int = 100, hi: int = 2048):
+def qwen3_decode_lengths(seed: int = 2, batch: int = 256, lo: int = 100, hi: int = 2048,
+                         rank: int = 0, world: int = 1):
     """Qwen3-0.6B-shaped decode batch: context lengths uniform in [lo, hi]."""
-    return rng(seed).integers(lo, hi + 1, size=batch).astype(np.int32)
+    ctx = rng(seed).integers(lo, hi + 1, size=batch * world).astype(np.int32)
+    return ctx[rank * batch:(rank + 1) * batch]
 
 
-def qwen3_decode_layout(num_blocks: int, seed: int = 2, batch: int = 256) -> DecodeLayout:
+def qwen3_decode_layout(num_blocks: int, seed: int = 2, batch: int = 256, rank: int = 0,
+                        world: int = 1) -> DecodeLayout:
+    """The decode batch of one GPU. With world > 1 the global batch is batch * world
+    sequences and GPU `rank` holds sequences [rank * batch, (rank + 1) * batch) in its own pool
+    (sequences are independent, so the units shard with no exchange)."""
     g = rng(seed)
-    ctx = g.integers(100, 2048 + 1, size=batch).astype(np.int32)
-    return decode_layout(ctx, num_blocks, g)
+    ctx = g.integers(100, 2048 + 1, size=batch * world).astype(np.int32)
+    return decode_layout(ctx[rank * batch:(rank + 1) * batch], num_blocks, g)
+
+
+def shard_range(units: int, rank: int, world: int) -> tuple[int, int]:
+    """Contiguous share [lo, hi) of `units` independent work units for one rank."""
+    per, extra = divmod(units, world)
+    lo = rank * per + min(rank, extra)
+    return lo, lo + per + (1 if rank < extra else 0)
 
 
 def long_decode_layout(num_blocks: int, seed: int = 5, batch: int = 32, ctx: int = 32768):
