@@ -148,8 +148,10 @@ def decode_bytes(ctx: np.ndarray, W: int) -> dict:
 # --------------------------------------------------------------------------- decode step
 class DecodeStep:
     def __init__(self, pkv, seed: int = 2, pool_fraction: float = 0.9, batch: int = B,
-                 num_blocks: int | None = None, rank: int = 0, world: int = 1):
+                 num_blocks: int | None = None, rank: int = 0, world: int = 1,
+                 layers: int = LAYERS):
         self.pkv = pkv
+        self.layers = layers
         free, _ = torch.cuda.mem_get_info()
         ctx = w.qwen3_decode_lengths(seed, batch, rank=rank, world=world)
         need = w.blocks_needed(ctx)
@@ -160,16 +162,16 @@ class DecodeStep:
         self.lay = w.qwen3_decode_layout(self.num_blocks, seed, batch, rank, world)
         lay = self.lay
         self.B = lay.batch
-        self.pool = torch.empty((2, LAYERS, self.num_blocks, BS, HKV, D), dtype=torch.bfloat16,
+        self.pool = torch.empty((2, layers, self.num_blocks, BS, HKV, D), dtype=torch.bfloat16,
                                 device="cuda")
         ids = torch.from_numpy(np.unique(lay.block_tables[lay.block_tables >= 0])).long().cuda()
-        for l in range(LAYERS):      # only referenced blocks hold data (untimed)
+        for l in range(layers):      # only referenced blocks hold data (untimed)
             for kv in range(2):
                 self.pool[kv, l][ids] = w.device_bf16_normal((len(ids), BS, HKV, D),
                                                              10_000 + 2 * l + kv)
-        self.q = w.device_bf16_normal((LAYERS, self.B, HQ, D), 20_001)
-        self.kn = w.device_bf16_normal((LAYERS, self.B, HKV, D), 20_002)
-        self.vn = w.device_bf16_normal((LAYERS, self.B, HKV, D), 20_003)
+        self.q = w.device_bf16_normal((layers, self.B, HQ, D), 20_001)
+        self.kn = w.device_bf16_normal((layers, self.B, HKV, D), 20_002)
+        self.vn = w.device_bf16_normal((layers, self.B, HKV, D), 20_003)
         self.out = torch.empty_like(self.q)
         self.slots = torch.from_numpy(lay.slot_mapping).cuda()
         self.tables = torch.from_numpy(lay.block_tables).cuda()
@@ -178,12 +180,12 @@ class DecodeStep:
         self.ws = pkv.decode_workspace(self.B, HQ, HKV, D, self.maxc, 0)
         self.splits_workspace = pkv.decode_workspace_bytes(self.B, HQ, HKV, D, self.maxc, 0)
         self.bytes = decode_bytes(lay.context_lens, lay.block_tables.shape[1])
-        self.step_bytes = LAYERS * (self.bytes["store"] + self.bytes["decode"])
-        self.kv_tokens = LAYERS * int(lay.context_lens.sum())
+        self.step_bytes = layers * (self.bytes["store"] + self.bytes["decode"])
+        self.kv_tokens = layers * int(lay.context_lens.sum())
 
     def run(self, events=None):
         pkv, s = self.pkv, self.pool
-        for l in range(LAYERS):
+        for l in range(self.layers):
             pkv.kv_store(self.kn[l], self.vn[l], self.slots, s[0, l], s[1, l])
             if events is not None:
                 events.append(torch.cuda.Event(enable_timing=True))
@@ -195,7 +197,7 @@ class DecodeStep:
                 events[-1].record()
 
     def launches_per_step(self):
-        return LAYERS * (2 + (1 if self.splits_workspace > 0 else 0))
+        return self.layers * (2 + (1 if self.splits_workspace > 0 else 0))
 
 
 def time_e2e(step: DecodeStep, steps: int):
@@ -335,17 +337,23 @@ def run_ours(args):
     if pkv.get_device_errors():
         raise RuntimeError("device error bits set during warm-up")
 
-    events = []
     with ClockSampler(torch.cuda.current_device()) as clocks:
+        # timed region 1: the headline, K steps back to back
         barrier(world)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         for _ in range(args.steps):
-            step.run(events)
+            step.run()
         e1.record()
         torch.cuda.synchronize()
         barrier(world)
+        # timed region 2: the same K steps with an event pair around every decode call, for
+        # the decode kernel's own launch duration (roofline)
+        events = []
+        for _ in range(args.steps):
+            step.run(events)
+        torch.cuda.synchronize()
     elapsed = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
     per_step = elapsed / args.steps
     decode_times = [a.elapsed_time(b) / 1e3 for a, b in zip(events[0::2], events[1::2])]
@@ -450,6 +458,48 @@ def run_reference(args):
     }), flush=True)
 
 
+def run_profile(args):
+    """One kernel alone on its workload, for ncu: `decode` (the Qwen3 batch, one layer, a pool
+    of just the referenced blocks: 1.2 GB, larger than L2), `prefill` (the varlen workload,
+    packed) or `store` (the varlen workload's kv_store). Runs --warmup + --steps launches."""
+    torch.cuda.set_device(0)
+    pkv = load_pkv()
+    if args.profile == "decode":
+        ctx = w.qwen3_decode_lengths()
+        step = DecodeStep(pkv, num_blocks=w.blocks_needed(ctx) + 8, layers=1)
+        s = step.pool
+        run = lambda: pkv.paged_decode_attn(step.q[0], s[0, 0], s[1, 0], step.tables, step.ctx,
+                                            step.maxc, step.lay.scale, workspace=step.ws,
+                                            out=step.out[0])
+    elif args.profile == "store":
+        lens = w.varlen_prefill_lengths()
+        lay = w.varlen_prefill_layout(num_blocks=w.blocks_needed(lens) + 64)
+        T = int(lens.sum())
+        k, v = (w.device_bf16_normal((T, HKV, D), 301 + i) for i in range(2))
+        kc = torch.empty((lay.num_blocks, BS, HKV, D), dtype=torch.bfloat16, device="cuda")
+        vc = torch.empty_like(kc)
+        slots = torch.from_numpy(lay.slot_mapping).cuda()
+        run = lambda: pkv.kv_store(k, v, slots, kc, vc)
+    else:
+        lens = w.varlen_prefill_lengths()
+        cu = torch.from_numpy(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)).cuda()
+        T = int(lens.sum())
+        q = w.device_bf16_normal((T, HQ, D), 401)
+        k = w.device_bf16_normal((T, HKV, D), 402)
+        v = w.device_bf16_normal((T, HKV, D), 403)
+        out = torch.empty_like(q)
+        mx = int(lens.max())
+        run = lambda: pkv.varlen_prefill_attn(q, k, v, cu, cu, mx, mx, D ** -0.5, out=out)
+    for _ in range(args.warmup + args.steps):
+        run()
+    torch.cuda.synchronize()
+    errors = pkv.get_device_errors()
+    print(json.dumps({"profile": args.profile, "launches": args.warmup + args.steps,
+                      "device_errors": errors}))
+    if errors:
+        sys.exit(1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -460,10 +510,14 @@ def main():
                     help="fraction of free HBM for the KV pool (the workload says 0.9)")
     ap.add_argument("--skip-extra", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--profile", choices=["decode", "prefill", "store"],
+                    help="run one kernel alone (for ncu); prints no benchmark line")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.profile:
+        run_profile(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

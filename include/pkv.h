@@ -56,7 +56,10 @@ typedef int32_t pkv_status;
 #define PKV_DEVERR_CONTEXT_RANGE 4u   /* decode: context_lens[b] < 0, > max_context_len,
                                          or > block_table_width * block_size */
 #define PKV_DEVERR_SEQLEN_RANGE 8u    /* prefill: bad cu_seqlens entry */
-#define PKV_DEVERR_TIMEOUT 16u        /* a pipeline wait gave up (the kernel returned early) */
+#define PKV_DEVERR_TIMEOUT 16u        /* a pipeline wait gave up after 2 s. The bit is sticky:
+                                         while it is set, every attention kernel of the library
+                                         returns at once without computing, until
+                                         pkv_get_device_errors(&e, 1) clears it. */
 
 /* Human-readable name of a status code. Never NULL; the string is static. */
 const char *pkv_status_string(pkv_status status);

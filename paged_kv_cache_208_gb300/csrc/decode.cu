@@ -108,7 +108,7 @@ __global__ void __maxnreg__(112)
     }
     fence_mbar_init();
   }
-  __syncthreads();
+  if (__syncthreads_or(threadIdx.x == 0 && aborted(err))) return;  // uniform across the CTA
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------------ producer
@@ -120,7 +120,7 @@ __global__ void __maxnreg__(112)
     int issued = 0;
     for (int it = 0; it < ntiles; ++it) {
       const int stage = it % kStages;
-      if (it >= kStages && !wait_parity(&sm.empty[stage], ((it / kStages) - 1) & 1)) {
+      if (it >= kStages && !wait_parity(&sm.empty[stage], ((it / kStages) - 1) & 1, err)) {
         record_error(err, 16u /* TIMEOUT */);
         break;
       }
@@ -140,7 +140,7 @@ __global__ void __maxnreg__(112)
     }
     // keep the CTA alive until every copy it issued has landed
     for (int it = max(0, issued - kStages); it < issued; ++it)
-      if (!wait_parity(&sm.full[it % kStages], (it / kStages) & 1)) {
+      if (!wait_parity(&sm.full[it % kStages], (it / kStages) & 1, err)) {
         record_error(err, 16u);
         break;
       }
@@ -180,10 +180,8 @@ __global__ void __maxnreg__(112)
 
   for (int it = 0; it < ntiles; ++it) {
     const int stage = it % kStages;
-    if (!wait_parity(&sm.full[stage], (it / kStages) & 1)) {
-      if (lane == 0) record_error(err, 16u);
-      break;
-    }
+    // warp-uniform: the loop body uses full-warp shuffles
+    if (!__all_sync(kFull, wait_parity(&sm.full[stage], (it / kStages) & 1, err))) break;
     const uint8_t *kt = sm.k[stage];
     const uint8_t *vt = sm.v[stage];
     const int tile_pos = tok_begin + it * kTile;

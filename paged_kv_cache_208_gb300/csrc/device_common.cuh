@@ -55,16 +55,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return done != 0;
 }
 
+constexpr unsigned int kErrTimeout = 16u;  // PKV_DEVERR_TIMEOUT
+
+// True once any kernel of the library has given up on a wait: every later wait and every
+// CTA that has not started yet returns at once, so one stuck pipeline cannot turn into
+// thousands of CTAs each waiting out the limit.
+__device__ __forceinline__ bool aborted(const unsigned int *err) {
+  return err && (*reinterpret_cast<const volatile unsigned int *>(err) & kErrTimeout);
+}
+
 // Wait until the phase with the given parity has completed. Returns false if it did not
-// complete within kWaitLimitNs.
-__device__ __forceinline__ bool wait_parity(uint64_t *bar, uint32_t parity) {
+// complete within kWaitLimitNs (then the timeout bit is set) or the abort bit is set.
+__device__ __forceinline__ bool wait_parity(uint64_t *bar, uint32_t parity, unsigned int *err) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (aborted(err)) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (err) atomicOr(err, kErrTimeout);
+      return false;
+    }
   }
 }
 

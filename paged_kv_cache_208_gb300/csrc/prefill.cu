@@ -129,6 +129,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   PrefillSmem &sm = *reinterpret_cast<PrefillSmem *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
+  // an earlier wait gave up somewhere: return before allocating anything (uniform)
+  if (__syncthreads_or(tid == 0 && aborted(p.err))) return;
   if (tid == 0) {
     mbar_init(&sm.q_full, 1);
     for (int i = 0; i < kStages; ++i) {
@@ -182,13 +184,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           row = (int32_t)(k0 + (int64_t)j * kBN);
         }
-        if (j >= kStages && !wait_parity(&sm.k_empty[st], ((j / kStages) - 1) & 1)) {
+        if (j >= kStages && !wait_parity(&sm.k_empty[st], ((j / kStages) - 1) & 1, p.err)) {
           ok = false;
           break;
         }
         mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
         tma_load_3d(sm.k[st], &kmap, &sm.k_full[st], 0, row, 2 * h, pol_kv);
-        if (j >= kStages && !wait_parity(&sm.v_empty[st], ((j / kStages) - 1) & 1)) {
+        if (j >= kStages && !wait_parity(&sm.v_empty[st], ((j / kStages) - 1) & 1, p.err)) {
           ok = false;
           issued = -(j + 1);  // K_j issued, V_j not
           break;
@@ -202,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     if (ok && fix_v) {
       const int j = nk - 1, st = j % kStages;
-      const bool landed = wait_parity(&sm.v_full[st], (j / kStages) & 1);
+      const bool landed = wait_parity(&sm.v_full[st], (j / kStages) & 1, p.err);
       if (landed) {
         uint8_t *vt = sm.v[st];
         for (int idx = lane; idx < (kBN - last_rows) * 16; idx += 32) {
@@ -220,11 +222,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {  // keep the CTA alive until every copy issued has landed
       const int kdone = issued >= 0 ? issued : -issued;
       const int vdone = issued >= 0 ? issued : -issued - 1;
-      bool drained = wait_parity(&sm.q_full, 0);
+      bool drained = wait_parity(&sm.q_full, 0, p.err);
       for (int j = max(0, kdone - kStages); drained && j < kdone; ++j)
-        drained = wait_parity(&sm.k_full[j % kStages], (j / kStages) & 1);
+        drained = wait_parity(&sm.k_full[j % kStages], (j / kStages) & 1, p.err);
       for (int j = max(0, vdone - kStages); drained && j < vdone; ++j)
-        drained = wait_parity(&sm.v_full[j % kStages], (j / kStages) & 1);
+        drained = wait_parity(&sm.v_full[j % kStages], (j / kStages) & 1, p.err);
       if (!drained) record_error(p.err, 16u);
     }
   } else if (warp == kMmaWarp) {
@@ -233,13 +235,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdS = idesc_bf16_f32(kBM, kBN, 0, 0);  // Q (K-major) x K (K-major)
       constexpr uint32_t kIdO = idesc_bf16_f32(kBM, kD, 0, 1);   // P (K-major) x V (MN-major)
       const uint32_t qa = smem_addr(sm.q), pa = smem_addr(sm.p);
-      bool ok = wait_parity(&sm.q_full, 0);
+      bool ok = wait_parity(&sm.q_full, 0, p.err);
       auto issue_pv = [&](int i) {
         if (!ok) return;
         const int st = i % kStages;
-        ok = wait_parity(&sm.p_full, i & 1) &&
-             ((i == nk - 1 && fix_v) ? wait_parity(&sm.v_fixed, 0)
-                                     : wait_parity(&sm.v_full[st], (i / kStages) & 1));
+        ok = wait_parity(&sm.p_full, i & 1, p.err) &&
+             ((i == nk - 1 && fix_v) ? wait_parity(&sm.v_fixed, 0, p.err)
+                                     : wait_parity(&sm.v_full[st], (i / kStages) & 1, p.err));
         if (!ok) return;
         tc_fence_after_sync();
         const uint32_t va = smem_addr(sm.v[st]);
@@ -254,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       for (int j = 0; j < nk && ok; ++j) {
         const int st = j % kStages;
-        ok = wait_parity(&sm.k_full[st], (j / kStages) & 1);
+        ok = wait_parity(&sm.k_full[st], (j / kStages) & 1, p.err);
         if (!ok) break;
         tc_fence_after_sync();
         const uint32_t ka = smem_addr(sm.k[st]);
@@ -271,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       issue_pv(nk - 1);
       // every UMMA must be complete before the tensor memory is released
-      if (!ok || !wait_parity(&sm.o_full, (nk - 1) & 1)) record_error(p.err, 16u);
+      if (!ok || !wait_parity(&sm.o_full, (nk - 1) & 1, p.err)) record_error(p.err, 16u);
     }
   } else {
     // ------------------------------------------------------------------ softmax warps
@@ -286,7 +288,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < nk; ++j) {
-      if (!wait_parity(&sm.s_full[j & 1], (j >> 1) & 1)) {
+      // warp-uniform results: the TMEM loads and stores below are .sync.aligned
+      if (!__all_sync(0xffffffffu, wait_parity(&sm.s_full[j & 1], (j >> 1) & 1, p.err))) {
         ok = false;
         break;
       }
@@ -333,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // P_{j-1} V_{j-1} must be done before P is overwritten and O is rescaled
       if (j >= 1) {
-        if (!wait_parity(&sm.o_full, (j - 1) & 1)) {
+        if (!__all_sync(0xffffffffu, wait_parity(&sm.o_full, (j - 1) & 1, p.err))) {
           ok = false;
           break;
         }
@@ -363,10 +366,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&sm.p_full);
     }
     // ---- epilogue: O / l -> bf16 rows
-    if (ok && !wait_parity(&sm.o_full, (nk - 1) & 1)) ok = false;
-    if (!ok) {
-      if (lane == 0) record_error(p.err, 16u);
-    } else {
+    if (ok) ok = __all_sync(0xffffffffu, wait_parity(&sm.o_full, (nk - 1) & 1, p.err));
+    if (ok) {
       tc_fence_after_sync();
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
       uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((q0 + qi) * p.num_q_heads + hq0 + g) * kD);
