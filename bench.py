@@ -149,9 +149,10 @@ def decode_bytes(ctx: np.ndarray, W: int) -> dict:
 class DecodeStep:
     def __init__(self, pkv, seed: int = 2, pool_fraction: float = 0.9, batch: int = B,
                  num_blocks: int | None = None, rank: int = 0, world: int = 1,
-                 layers: int = LAYERS):
+                 layers: int = LAYERS, num_splits: int = 0):
         self.pkv = pkv
         self.layers = layers
+        self.num_splits = num_splits
         free, _ = torch.cuda.mem_get_info()
         ctx = w.qwen3_decode_lengths(seed, batch, rank=rank, world=world)
         need = w.blocks_needed(ctx)
@@ -177,8 +178,9 @@ class DecodeStep:
         self.tables = torch.from_numpy(lay.block_tables).cuda()
         self.ctx = torch.from_numpy(lay.context_lens).cuda()
         self.maxc = lay.max_context_len
-        self.ws = pkv.decode_workspace(self.B, HQ, HKV, D, self.maxc, 0)
-        self.splits_workspace = pkv.decode_workspace_bytes(self.B, HQ, HKV, D, self.maxc, 0)
+        self.ws = pkv.decode_workspace(self.B, HQ, HKV, D, self.maxc, num_splits)
+        self.splits_workspace = pkv.decode_workspace_bytes(self.B, HQ, HKV, D, self.maxc,
+                                                           num_splits)
         self.bytes = decode_bytes(lay.context_lens, lay.block_tables.shape[1])
         self.step_bytes = layers * (self.bytes["store"] + self.bytes["decode"])
         self.kv_tokens = layers * int(lay.context_lens.sum())
@@ -191,7 +193,8 @@ class DecodeStep:
                 events.append(torch.cuda.Event(enable_timing=True))
                 events[-1].record()
             pkv.paged_decode_attn(self.q[l], s[0, l], s[1, l], self.tables, self.ctx, self.maxc,
-                                  self.lay.scale, workspace=self.ws, out=self.out[l])
+                                  self.lay.scale, num_splits=self.num_splits, workspace=self.ws,
+                                  out=self.out[l])
             if events is not None:
                 events.append(torch.cuda.Event(enable_timing=True))
                 events[-1].record()
@@ -330,7 +333,8 @@ def run_ours(args):
     pkv = load_pkv()
     hbm_peak, bf16_peak, bf16_sus, peak_src = peaks()
 
-    step = DecodeStep(pkv, pool_fraction=args.pool_fraction, rank=rank, world=world)
+    step = DecodeStep(pkv, pool_fraction=args.pool_fraction, rank=rank, world=world,
+                      num_splits=args.num_splits)
     for _ in range(args.warmup):
         step.run()
     torch.cuda.synchronize()
@@ -401,7 +405,7 @@ def run_ours(args):
         "config": {"workload": WORKLOAD, "batch": step.B, "layers": LAYERS,
                    "sum_ctx": int(step.lay.context_lens.sum()), "num_blocks": step.num_blocks,
                    "pool_gb": round(step.pool.numel() * 2 / 1e9, 1),
-                   "splits": "auto", "l2": "inputs larger than L2 (1.13 GB of KV per layer)",
+                   "splits": args.num_splits or "auto", "l2": "inputs larger than L2 (1.13 GB of KV per layer)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "kv_tokens_per_s": step.kv_tokens * world / per_step,
         "decode_frac_of_hbm_peak": achieved / hbm_peak,
@@ -466,10 +470,12 @@ def run_profile(args):
     pkv = load_pkv()
     if args.profile == "decode":
         ctx = w.qwen3_decode_lengths()
-        step = DecodeStep(pkv, num_blocks=w.blocks_needed(ctx) + 8, layers=1)
+        step = DecodeStep(pkv, num_blocks=w.blocks_needed(ctx) + 8, layers=1,
+                          num_splits=args.num_splits)
         s = step.pool
         run = lambda: pkv.paged_decode_attn(step.q[0], s[0, 0], s[1, 0], step.tables, step.ctx,
-                                            step.maxc, step.lay.scale, workspace=step.ws,
+                                            step.maxc, step.lay.scale,
+                                            num_splits=args.num_splits, workspace=step.ws,
                                             out=step.out[0])
     elif args.profile == "store":
         lens = w.varlen_prefill_lengths()
@@ -510,6 +516,8 @@ def main():
                     help="fraction of free HBM for the KV pool (the workload says 0.9)")
     ap.add_argument("--skip-extra", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--num-splits", type=int, default=0,
+                    help="decode KV splits of the longest context (0 = the library's choice)")
     ap.add_argument("--profile", choices=["decode", "prefill", "store"],
                     help="run one kernel alone (for ncu); prints no benchmark line")
     args = ap.parse_args()
