@@ -203,6 +203,43 @@ pkv_status pkv_varlen_prefill_attn(const void *q, int64_t q_tok_stride, int64_t 
                                    int32_t causal, void *workspace, size_t workspace_bytes,
                                    void *out, void *stream);
 
+/*
+ * paged_decode_attn_noalloc -- the same computation as pkv_paged_decode_attn, for callers
+ * that cannot allocate device memory. (The nano-vLLM pages have no counterpart: this entry
+ * point exists for library users, not for the method.)
+ *
+ * Who needs it: code that has no way to get a workspace at call time -- e.g. a plug-in in a
+ * serving engine that has already given nearly all of HBM to its KV pool and offers kernels
+ * no allocator, or a call site where cudaMalloc is not allowed (it synchronises the device,
+ * and it is forbidden while a stream is being captured).
+ *
+ * Arguments are those of pkv_paged_decode_attn without workspace / workspace_bytes; the
+ * caller still owns q, the pools, the tables and out. The split-K partial results live in a
+ * fixed array of PKV_DECODE_NOALLOC_SCRATCH_BYTES bytes that belongs to the library's device
+ * image, so every device that uses it holds that memory until the process exits. The split
+ * plan is the one pkv_paged_decode_attn would use (same num_splits rule), so for the same
+ * inputs the two entry points compute the same result. A problem whose plan needs more than
+ * the array (pkv_decode_workspace_bytes(...) > PKV_DECODE_NOALLOC_SCRATCH_BYTES) is rejected
+ * with PKV_ERR_WORKSPACE before anything is enqueued; choosing fewer splits (num_splits > 0)
+ * or the workspace entry point avoids that. The automatic plan of the Qwen3-shaped batch (256
+ * sequences x 16 query heads, contexts up to 2048) needs about 17 MB.
+ *
+ * The first call on each device looks up the array's device address (cudaGetSymbolAddress,
+ * with that device current) and caches it; make that first call before any stream capture.
+ * All calls on a device share the array and it keeps the last call's contents (nothing needs
+ * to start at zero). Calls whose kernels may run at the same time on the GPU (different
+ * streams without ordering) race on the array: order them on one stream.
+ */
+#define PKV_DECODE_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+pkv_status pkv_paged_decode_attn_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                                         const int32_t *block_tables, int32_t block_table_width,
+                                         const int32_t *context_lens, int32_t batch,
+                                         int32_t max_context_len, int32_t num_q_heads,
+                                         int32_t num_kv_heads, int32_t head_dim,
+                                         int32_t block_size, int64_t num_blocks, float scale,
+                                         int32_t num_splits, void *out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

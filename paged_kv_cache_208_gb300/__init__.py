@@ -34,6 +34,8 @@ SIGNATURES = {
     "pkv_decode_workspace_bytes": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32]),
     "pkv_paged_decode_attn": (_I32, [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32,
                                      _I32, _I64, _F, _I32, _P, _SZ, _P, _P]),
+    "pkv_paged_decode_attn_noalloc": (_I32, [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32,
+                                             _I32, _I32, _I64, _F, _I32, _P, _P]),
     "pkv_prefill_workspace_bytes": (_SZ, [_I32, _I32, _I32, _I32]),
     "pkv_varlen_prefill_attn": (_I32, [_P, _I64, _I64, _P, _P, _I64, _I64, _P, _P, _I32, _I32,
                                        _I32, _P, _I32, _I32, _I64, _I32, _I32, _I32, _F, _I32,
@@ -156,6 +158,31 @@ def paged_decode_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
         _ptr(context_lens), B, int(max_context_len), hq, hkv, d, bs, nb, float(scale),
         int(num_splits), _ptr(workspace), workspace.numel(), _ptr(out), _stream(stream)))
+    return out
+
+
+def paged_decode_attn_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                              block_tables: torch.Tensor, context_lens: torch.Tensor,
+                              max_context_len: int, scale: float, num_splits: int = 0,
+                              out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """paged_decode_attn without a workspace argument, for callers that cannot allocate
+    device memory: the split results go to a fixed array inside the library (see pkv.h).
+    Calls on one device must not overlap on the GPU."""
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, torch.bfloat16)
+    _need(block_tables, "block_tables", torch.int32)
+    _need(context_lens, "context_lens", torch.int32)
+    if not (q.is_contiguous() and k_cache.is_contiguous() and v_cache.is_contiguous()
+            and block_tables.is_contiguous() and context_lens.is_contiguous()):
+        raise ValueError("q, caches, block_tables and context_lens must be contiguous")
+    B, hq, d = q.shape
+    nb, bs, hkv, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _check("pkv_paged_decode_attn_noalloc", _LIB.pkv_paged_decode_attn_noalloc(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+        _ptr(context_lens), B, int(max_context_len), hq, hkv, d, bs, nb, float(scale),
+        int(num_splits), _ptr(out), _stream(stream)))
     return out
 
 

@@ -76,6 +76,11 @@ struct PrefillArgs {
 cudaError_t launch_varlen_prefill(const PrefillArgs &a, int num_sms, cudaStream_t stream);
 bool prefill_group_supported(int group);  // num_q_heads / num_kv_heads
 
+// the current device's SM count and the address of the device error word (pkv_api.cu);
+// 0 / nullptr when the CUDA runtime cannot answer
+int current_sm_count();
+unsigned int *current_error_word();
+
 // tensor maps (pkv_api.cu): the driver's cuTensorMapEncodeTiled, fetched at run time
 CUresult encode_tensor_map(CUtensorMap *map, CUtensorMapDataType dtype, uint32_t rank,
                            void *base, const uint64_t *dims, const uint64_t *strides_bytes,

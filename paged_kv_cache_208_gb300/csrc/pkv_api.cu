@@ -70,6 +70,16 @@ pkv_status launch_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV
 
 namespace pkv {
 
+int current_sm_count() {
+  DeviceInfo *d = device_info();
+  return d ? d->num_sms : 0;
+}
+
+unsigned int *current_error_word() {
+  DeviceInfo *d = device_info();
+  return d ? d->err : nullptr;
+}
+
 CUresult encode_tensor_map(CUtensorMap *map, CUtensorMapDataType dtype, uint32_t rank,
                            void *base, const uint64_t *dims, const uint64_t *strides_bytes,
                            const uint32_t *box, CUtensorMapSwizzle swizzle,
