@@ -7,7 +7,8 @@
 // Work unit (one CTA): sequence b, KV head h, up to two of the G query heads of h (so a
 // CTA reads each K/V byte once for both heads of a Qwen3 group), and one split: the
 // logical tokens [s * chunk, min((s + 1) * chunk, ctx_b)). chunk is a multiple of the 64-
-// token tile and the block size is a multiple of 256, so a tile never straddles a block.
+// token tile (up to 1024 tokens when there is enough parallelism) and the block size is a
+// multiple of 256, so a tile never straddles a block.
 //
 // Pipeline (per CTA, 8 consumer warps + 1 producer warp):
 //   producer  -- one thread looks up block_tables[b][pos / block_size] and issues two TMA
@@ -15,8 +16,10 @@
 //                128-byte swizzled) into a 3-stage ring guarded by full/empty mbarriers;
 //   consumers -- warp w owns tokens [8w, 8w + 8) of every tile and keeps its own online-
 //                softmax state (running max m, sum l, accumulator acc) in registers:
-//                  QK:  4 lanes per token, 32 dims per lane, reduced with 2 shuffles;
-//                  PV:  16 lanes per token (8 dims each), two tokens per instruction;
+//                  QK:  4 lanes per token, 32 dims per lane, mixed-precision bf16 FMAs on
+//                       packed q (no conversions), reduced with 2 shuffles;
+//                  PV:  16 lanes per token (8 dims each), two tokens per instruction,
+//                       packed fp32x2 FMAs;
 //                at the end the 8 warp states are merged through shared memory.
 // With one split the CTA writes bf16 output directly; otherwise it writes its normalised
 // partial output and log2-sum-exp, and decode_combine_kernel merges the splits.
@@ -61,8 +64,9 @@ __device__ __forceinline__ uint32_t tile_offset(int t, int j) {
 }
 
 template <int GC>
-// 112 registers: two 288-thread CTAs (104 KiB of shared memory each) fit on one SM.
-__global__ void __maxnreg__(112)
+// 96 registers: warps are placed on the 4 SM sub-partitions (16K registers each), so two
+// 9-warp CTAs (5 warps on some sub-partitions) fit only at <= 102 registers per thread.
+__global__ void __maxnreg__(96)
     decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const uint16_t *__restrict__ q,
                         const int32_t *__restrict__ block_tables, int32_t table_width,
@@ -148,34 +152,46 @@ __global__ void __maxnreg__(112)
   }
 
   // -------------------------------------------------------------------- consumers
-  const int tq = lane >> 2;   // QK: token within the warp's 8
-  const int qc = lane & 3;    // QK: quarter -> chunks qc, qc+4, qc+8, qc+12
+  // QK: 4 lanes per token. Lane = (tq & 3) + 4 sub + 16 (tq >> 2): token tq of the warp's 8,
+  // sub selects chunks {r, r+8, r+4, r+12}[sub] for r = 0..3. A quarter-warp (8 lanes, one
+  // 128-bit shared-memory phase) then reads 4 tokens x chunks {c, c + 8}, which sit in
+  // different swizzle rows, so its 8 accesses hit 8 distinct bank groups.
+  const int tq = (lane & 3) | ((lane >> 4) << 2);
+  const int sub = (lane >> 2) & 3;
   const int hw = lane >> 4;   // PV: token parity
   const int dl = lane & 15;   // PV: chunk (dims 8dl..8dl+7)
+  const int t_qk = warp * 8 + tq;
+  const int chunk0 = 8 * (sub & 1) + 4 * (sub >> 1);  // chunks chunk0 + r, r = 0..3
+  // shared-memory offsets inside a tile are the same for every tile
+  uint32_t off_qk[4], off_pv[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) off_qk[r] = tile_offset(t_qk, chunk0 + r);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) off_pv[i] = tile_offset(warp * 8 + 2 * i + hw, dl);
 
-  float qr[GC][4][8];
+  // q stays packed bf16: QK uses mixed-precision FMAs, the scale is applied to the score
+  uint32_t qw[GC][4][4];
 #pragma unroll
   for (int g = 0; g < GC; ++g) {
     const uint4 *qrow = reinterpret_cast<const uint4 *>(q + ((int64_t)b * num_q_heads + hq0 + g) * kD);
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-      const uint4 w4 = __ldg(qrow + qc + 4 * r);
-      const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        qr[g][r][2 * e] = bf16_lo(w[e]) * qscale;
-        qr[g][r][2 * e + 1] = bf16_hi(w[e]) * qscale;
-      }
+      const uint4 w4 = __ldg(qrow + chunk0 + r);
+      qw[g][r][0] = w4.x;
+      qw[g][r][1] = w4.y;
+      qw[g][r][2] = w4.z;
+      qw[g][r][3] = w4.w;
     }
   }
 
-  float m_run[GC], l_run[GC], acc[GC][8];
+  float m_run[GC], l_run[GC];
+  float2 acc[GC][4];  // dims 8dl + 2e, 8dl + 2e + 1
 #pragma unroll
   for (int g = 0; g < GC; ++g) {
     m_run[g] = -INFINITY;
     l_run[g] = 0.f;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[g][e] = 0.f;
+    for (int e = 0; e < 4; ++e) acc[g][e] = make_float2(0.f, 0.f);
   }
 
   for (int it = 0; it < ntiles; ++it) {
@@ -184,33 +200,35 @@ __global__ void __maxnreg__(112)
     if (!__all_sync(kFull, wait_parity(&sm.full[stage], (it / kStages) & 1, err))) break;
     const uint8_t *kt = sm.k[stage];
     const uint8_t *vt = sm.v[stage];
-    const int tile_pos = tok_begin + it * kTile;
-    const int n_valid = tok_end - tile_pos;  // tokens of this tile inside the split (>= 1)
+    const int n_valid = tok_end - (tok_begin + it * kTile);  // >= 1; < 64 only in a last tile
 
-    // ---- scores for token t = 8 warp + tq (log2 domain: q carries scale * log2 e)
-    const int t = warp * 8 + tq;
+    // ---- scores for token t_qk (log2 domain)
     float sc[GC];
+    {
+      float s_lo[GC], s_hi[GC];
 #pragma unroll
-    for (int g = 0; g < GC; ++g) sc[g] = 0.f;
+      for (int g = 0; g < GC; ++g) s_lo[g] = s_hi[g] = 0.f;
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const uint4 k4 = *reinterpret_cast<const uint4 *>(kt + tile_offset(t, qc + 4 * r));
-      const uint32_t w[4] = {k4.x, k4.y, k4.z, k4.w};
+      for (int r = 0; r < 4; ++r) {
+        const uint4 k4 = *reinterpret_cast<const uint4 *>(kt + off_qk[r]);
+        const uint32_t w[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float k0 = bf16_lo(w[e]), k1 = bf16_hi(w[e]);
+        for (int e = 0; e < 4; ++e)
 #pragma unroll
-        for (int g = 0; g < GC; ++g) {
-          sc[g] = fmaf(qr[g][r][2 * e], k0, sc[g]);
-          sc[g] = fmaf(qr[g][r][2 * e + 1], k1, sc[g]);
-        }
+          for (int g = 0; g < GC; ++g) fma_bf16_pairs(qw[g][r][e], w[e], s_lo[g], s_hi[g]);
+      }
+#pragma unroll
+      for (int g = 0; g < GC; ++g) {
+        float v = s_lo[g] + s_hi[g];
+        v += __shfl_xor_sync(kFull, v, 4);   // the 4 lanes of a token differ in lane bits 2-3
+        v += __shfl_xor_sync(kFull, v, 8);
+        sc[g] = v * qscale;
       }
     }
+    if (n_valid < kTile) {
 #pragma unroll
-    for (int g = 0; g < GC; ++g) {
-      sc[g] += __shfl_xor_sync(kFull, sc[g], 1);
-      sc[g] += __shfl_xor_sync(kFull, sc[g], 2);
-      if (t >= n_valid) sc[g] = -INFINITY;
+      for (int g = 0; g < GC; ++g)
+        if (t_qk >= n_valid) sc[g] = -INFINITY;
     }
 
     // ---- online softmax over the warp's 8 tokens
@@ -218,23 +236,28 @@ __global__ void __maxnreg__(112)
     bool any = false;
 #pragma unroll
     for (int g = 0; g < GC; ++g) {
-      float mx = sc[g];
-      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
-      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+      float mx = sc[g];  // the warp's 8 tokens differ in lane bits 0, 1 and 4
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
       mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
-      const float m_new = fmaxf(m_run[g], mx);
-      if (m_new != -INFINITY) {
-        any = true;
-        const float alpha = fast_exp2(m_run[g] - m_new);
-        p[g] = fast_exp2(sc[g] - m_new);
-        float ps = p[g];
-        ps += __shfl_xor_sync(kFull, ps, 4);
-        ps += __shfl_xor_sync(kFull, ps, 8);
-        ps += __shfl_xor_sync(kFull, ps, 16);
-        l_run[g] = l_run[g] * alpha + ps;
-        m_run[g] = m_new;
+      if (mx > m_run[g]) {  // warp-uniform: every lane holds the same maxima
+        const float alpha = fast_exp2(m_run[g] - mx);
+        l_run[g] *= alpha;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[g][e] *= alpha;
+        for (int e = 0; e < 4; ++e) {
+          acc[g][e].x *= alpha;
+          acc[g][e].y *= alpha;
+        }
+        m_run[g] = mx;
+      }
+      if (m_run[g] != -INFINITY) {
+        any = true;
+        p[g] = fast_exp2(sc[g] - m_run[g]);
+        float ps = p[g];
+        ps += __shfl_xor_sync(kFull, ps, 1);
+        ps += __shfl_xor_sync(kFull, ps, 2);
+        ps += __shfl_xor_sync(kFull, ps, 16);
+        l_run[g] += ps;
       } else {
         p[g] = 0.f;
       }
@@ -242,25 +265,23 @@ __global__ void __maxnreg__(112)
 
     // ---- acc += p v, two tokens per instruction (half-warp hw takes token 2i + hw)
     if (any) {
-      const bool full_tile = n_valid >= kTile;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int tt = 2 * i + hw;
-        float pv[GC];
+        float2 pv[GC];
 #pragma unroll
-        for (int g = 0; g < GC; ++g) pv[g] = __shfl_sync(kFull, p[g], 4 * tt);
-        const int t2 = warp * 8 + tt;
-        if (full_tile || t2 < n_valid) {
-          const uint4 v4 = *reinterpret_cast<const uint4 *>(vt + tile_offset(t2, dl));
+        for (int g = 0; g < GC; ++g) {
+          const float x = __shfl_sync(kFull, p[g], (tt & 3) | ((tt >> 2) << 4));
+          pv[g] = make_float2(x, x);
+        }
+        if (n_valid >= kTile || warp * 8 + tt < n_valid) {
+          const uint4 v4 = *reinterpret_cast<const uint4 *>(vt + off_pv[i]);
           const uint32_t w[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float v0 = bf16_lo(w[e]), v1 = bf16_hi(w[e]);
+            const float2 vf = make_float2(bf16_lo(w[e]), bf16_hi(w[e]));
 #pragma unroll
-            for (int g = 0; g < GC; ++g) {
-              acc[g][2 * e] = fmaf(pv[g], v0, acc[g][2 * e]);
-              acc[g][2 * e + 1] = fmaf(pv[g], v1, acc[g][2 * e + 1]);
-            }
+            for (int g = 0; g < GC; ++g) acc[g][e] = ffma2(pv[g], vf, acc[g][e]);
           }
         }
       }
@@ -273,12 +294,17 @@ __global__ void __maxnreg__(112)
 #pragma unroll
   for (int g = 0; g < GC; ++g)
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[g][e] += __shfl_xor_sync(kFull, acc[g][e], 16);
+    for (int e = 0; e < 4; ++e) {
+      acc[g][e].x += __shfl_xor_sync(kFull, acc[g][e].x, 16);
+      acc[g][e].y += __shfl_xor_sync(kFull, acc[g][e].y, 16);
+    }
   if (lane < 16) {
 #pragma unroll
-    for (int g = 0; g < GC; ++g)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) sm.acc[warp][g][8 * dl + e] = acc[g][e];
+    for (int g = 0; g < GC; ++g) {
+      float4 *dst = reinterpret_cast<float4 *>(&sm.acc[warp][g][8 * dl]);
+      dst[0] = make_float4(acc[g][0].x, acc[g][0].y, acc[g][1].x, acc[g][1].y);
+      dst[1] = make_float4(acc[g][2].x, acc[g][2].y, acc[g][3].x, acc[g][3].y);
+    }
   }
   if (lane == 0) {
 #pragma unroll
@@ -367,6 +393,11 @@ cudaError_t launch_split(const DecodeArgs &a, const DecodePlan &p, const CUtenso
     cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<GC>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    // all of the unified L1/shared storage as shared memory, so two CTAs fit on an SM
+    e = cudaFuncSetAttribute(decode_split_kernel<GC>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
   const dim3 grid(a.num_kv_heads * p.head_groups, p.splits, a.batch);
@@ -393,11 +424,11 @@ DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
     const int64_t per = (max_ctx + S - 1) / S;
     p.chunk = (int32_t)((per + kTile - 1) / kTile * kTile);
   } else {
-    // Smallest chunk (down to one tile) that still gives >= 8 CTAs per SM, capped at 4 tiles
-    // so that long and short contexts balance across the machine.
+    // Long chunks amortise a CTA's start-up (pipeline fill, q load, merge): take the longest
+    // chunk, up to 16 tiles, that still leaves >= 4 waves of CTAs (two per SM) for balance.
     const int64_t units = (int64_t)batch * num_kv_heads * p.head_groups;
-    const int64_t target = (int64_t)num_sms * 8;
-    int64_t chunk = 4 * kTile;
+    const int64_t target = (int64_t)num_sms * 2 * 4;
+    int64_t chunk = 16 * kTile;
     while (chunk > kTile && units * ((max_ctx + chunk - 1) / chunk) < target) chunk -= kTile;
     p.chunk = (int32_t)chunk;
   }

@@ -124,6 +124,34 @@ __device__ __forceinline__ float fast_exp2(float x) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// acc_lo += a.lo * b.lo and acc_hi += a.hi * b.hi for two packed bf16 pairs, each product
+// formed exactly and added to the fp32 accumulator with one rounding (mixed-precision FMA:
+// no conversion instructions).
+__device__ __forceinline__ void fma_bf16_pairs(uint32_t a, uint32_t b, float &acc_lo,
+                                               float &acc_hi) {
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+      "mov.b32 {al, ah}, %2;\n\t"
+      "mov.b32 {bl, bh}, %3;\n\t"
+      "fma.rn.f32.bf16 %0, al, bl, %0;\n\t"
+      "fma.rn.f32.bf16 %1, ah, bh, %1;\n\t}"
+      : "+f"(acc_lo), "+f"(acc_hi)
+      : "r"(a), "r"(b));
+}
+
+// Packed fp32 FMA on two lanes: d = a * b + c elementwise (one instruction).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
 __device__ __forceinline__ uint16_t bf16_bits_rn(float x) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(x));
 }

@@ -53,16 +53,16 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
 
 
 def test_noalloc_rejects_plans_larger_than_its_array():
-    """32 sequences x 32768 tokens split automatically need more than the array holds: the
+    """32 sequences x 32768 tokens cut into 256 splits need more than the array holds: the
     call is refused before anything runs (the tables only name block 0, and every context is
     1 token, so nothing could be read out of bounds even if it ran)."""
-    B, maxc = 32, 32768
-    assert pkv.decode_workspace_bytes(B, 16, 8, 128, maxc) > SCRATCH_BYTES
+    B, maxc, splits = 32, 32768, 256
+    assert pkv.decode_workspace_bytes(B, 16, 8, 128, maxc, splits) > SCRATCH_BYTES
     q = torch.zeros((B, 16, 128), dtype=torch.bfloat16, device="cuda")
     kc = torch.zeros((4, 256, 8, 128), dtype=torch.bfloat16, device="cuda")
     bt = torch.zeros((B, 128), dtype=torch.int32, device="cuda")
     cl = torch.ones(B, dtype=torch.int32, device="cuda")
     out = torch.full_like(q, 3.0)
-    assert _noalloc(q, kc, kc, bt, cl, maxc, 0.088, 0, out) == pkv.ERR_WORKSPACE
+    assert _noalloc(q, kc, kc, bt, cl, maxc, 0.088, splits, out) == pkv.ERR_WORKSPACE
     torch.cuda.synchronize()
     assert bool((out == 3.0).all())
