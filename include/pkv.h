@@ -152,9 +152,9 @@ pkv_status pkv_paged_decode_attn(const void *q, const void *k_cache, const void 
                                  void *stream);
 
 /*
- * Bytes of device workspace that pkv_varlen_prefill_attn needs (currently 0 for every
- * size; the argument pair is kept so that a scheduler state can be added without an ABI
- * change).
+ * Bytes of device workspace that pkv_varlen_prefill_attn needs: 16 for every size (the
+ * persistent kernel's work counter, which the call resets on its stream before the kernel
+ * runs). Returns 0 for invalid sizes.
  */
 size_t pkv_prefill_workspace_bytes(int32_t num_seqs, int32_t max_seqlen_q,
                                    int32_t num_q_heads, int32_t head_dim);
@@ -187,6 +187,8 @@ size_t pkv_prefill_workspace_bytes(int32_t num_seqs, int32_t max_seqlen_q,
  * cu_seqlens_q, cu_seqlens_k: [num_seqs + 1] int32, non-decreasing, starting at 0.
  * max_seqlen_q, max_seqlen_k: upper bounds of Lq and Lk over the batch.
  * block_table:   NULL, or [num_seqs, block_table_width] int32.
+ * workspace:     pkv_prefill_workspace_bytes(...) bytes, 16-byte aligned, private to this
+ *                call while it runs (two calls that may overlap need two workspaces).
  * out:           [Tq, num_q_heads, head_dim] bf16, contiguous.
  * Implemented: head_dim == 128, block_size a multiple of 256 when block_table is given,
  * num_q_heads / num_kv_heads in {1, 2, 4, 8}, token strides that are multiples of 8 elements, and

@@ -190,9 +190,11 @@ def varlen_prefill_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                         cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor,
                         max_seqlen_q: int, max_seqlen_k: int, scale: float, causal: bool = True,
                         block_table: torch.Tensor | None = None,
-                        out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+                        out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                        stream=None) -> torch.Tensor:
     """Causal attention over cu_seqlens-packed sequences. q: [Tq, Hq, D]; k, v: packed
-    [Tk, Hkv, D], or the pools [NB, bs, Hkv, D] when block_table [N, W] int32 is given."""
+    [Tk, Hkv, D], or the pools [NB, bs, Hkv, D] when block_table [N, W] int32 is given.
+    workspace: pkv_prefill_workspace_bytes bytes (allocated per call when omitted)."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, n, torch.bfloat16)
     _need(cu_seqlens_q, "cu_seqlens_q", torch.int32)
@@ -214,9 +216,13 @@ def varlen_prefill_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     if out is None:
         out = torch.empty((tq, hq, d), dtype=q.dtype, device=q.device)
     n = cu_seqlens_q.shape[0] - 1
+    if workspace is None:
+        workspace = torch.empty(max(16, int(_LIB.pkv_prefill_workspace_bytes(n, int(max_seqlen_q),
+                                                                          hq, d))),
+                                dtype=torch.uint8, device=q.device)
     _check("pkv_varlen_prefill_attn", _LIB.pkv_varlen_prefill_attn(
         _ptr(q), q.stride(0), tq, _ptr(k), _ptr(v), kv_stride, total_k,
         _ptr(cu_seqlens_q.contiguous()), _ptr(cu_seqlens_k.contiguous()), n, int(max_seqlen_q),
         int(max_seqlen_k), _ptr(block_table), W, bs, nb, hq, hkv, d, float(scale),
-        int(bool(causal)), None, 0, _ptr(out), _stream(stream)))
+        int(bool(causal)), _ptr(workspace), workspace.numel(), _ptr(out), _stream(stream)))
     return out

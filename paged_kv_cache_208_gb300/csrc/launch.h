@@ -71,8 +71,10 @@ struct PrefillArgs {
   float scale;
   int32_t causal;
   void *out;
+  void *workspace;   // kPrefillWorkspaceBytes: the persistent kernel's work counter
   unsigned int *err;
 };
+constexpr size_t kPrefillWorkspaceBytes = 16;
 cudaError_t launch_varlen_prefill(const PrefillArgs &a, int num_sms, cudaStream_t stream);
 bool prefill_group_supported(int group);  // num_q_heads / num_kv_heads
 

@@ -194,11 +194,8 @@ pkv_status pkv_paged_decode_attn(const void *q, const void *k_cache, const void 
 
 size_t pkv_prefill_workspace_bytes(int32_t num_seqs, int32_t max_seqlen_q, int32_t num_q_heads,
                                    int32_t head_dim) {
-  (void)num_seqs;
-  (void)max_seqlen_q;
-  (void)num_q_heads;
-  (void)head_dim;
-  return 0;
+  if (num_seqs < 0 || max_seqlen_q < 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
+  return pkv::kPrefillWorkspaceBytes;
 }
 
 pkv_status pkv_varlen_prefill_attn(const void *q, int64_t q_tok_stride, int64_t total_q,
@@ -211,8 +208,6 @@ pkv_status pkv_varlen_prefill_attn(const void *q, int64_t q_tok_stride, int64_t 
                                    int32_t num_kv_heads, int32_t head_dim, float scale,
                                    int32_t causal, void *workspace, size_t workspace_bytes,
                                    void *out, void *stream) {
-  (void)workspace;
-  (void)workspace_bytes;
   if (num_seqs < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || num_q_heads <= 0 ||
       num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || head_dim <= 0 ||
       !isfinite(scale))
@@ -234,6 +229,8 @@ pkv_status pkv_varlen_prefill_attn(const void *q, int64_t q_tok_stride, int64_t 
   if (q_tok_stride % 8 != 0 || kv_tok_stride % 8 != 0 || !aligned16(q) || !aligned16(k) ||
       !aligned16(v) || !aligned16(out))
     return PKV_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < pkv::kPrefillWorkspaceBytes || !aligned16(workspace))
+    return PKV_ERR_WORKSPACE;
   DeviceInfo *dev = device_info();
   if (!dev) return PKV_ERR_CUDA;
   pkv::PrefillArgs a{};
@@ -258,6 +255,7 @@ pkv_status pkv_varlen_prefill_attn(const void *q, int64_t q_tok_stride, int64_t 
   a.scale = scale;
   a.causal = causal;
   a.out = out;
+  a.workspace = workspace;
   a.err = dev->err;
   return launch_status(pkv::launch_varlen_prefill(a, dev->num_sms,
                                                   static_cast<cudaStream_t>(stream)));

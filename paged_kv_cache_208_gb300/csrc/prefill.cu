@@ -2,23 +2,29 @@
 //
 // flash_attn_varlen_func of «nano-vLLM 最小化vLLM重新实现», 架构 5: causal attention over
 // cu_seqlens-packed prompts, keys either packed or read from the paged pool through a block
-// table (prefix caching, where queries cover only the uncached suffix and the causal mask is
+// table (prefix caching: queries cover only the uncached suffix and the causal mask is
 // aligned to the end of the keys).
 //
-// Work unit (one CTA): sequence n, KV head h and a tile of 128 rows = the G query heads of h
-// (G = Hq / Hkv) x 128/G consecutive query tokens, so every K/V tile loaded serves all G
-// heads. For each 128-key tile j of the visible keys:
-//   S_j = Q K_j^T   (tcgen05.mma, A = Q and B = K_j from shared memory, S_j in TMEM)
-//   softmax warps: S_j row -> registers (tcgen05.ld), scale, causal mask, online max/sum in
-//                  the log2 domain, P_j = 2^(s - m) as bf16 into shared memory
-//   O += P_j V_j    (tcgen05.mma, A = P_j, B = V_j (MN-major), O accumulated in TMEM)
-// O is rescaled in TMEM only when a row's running max grows by more than 2^8 (the sum l
-// carries the same stale max, so O / l is unchanged).
+// Persistent kernel: one CTA per SM takes work items from a global queue (one atomic counter
+// in the caller's workspace; items ordered longest first, so the queue balances the SMs). The
+// producer warp takes the items and hands their ids to the other warps through a small ring
+// in shared memory. An item is
+// one sequence n, one KV head h and two 128-row M-tiles that share every K/V tile: for a GQA
+// group of two (or a pair of heads of a larger group) the two query heads over the same 128
+// tokens; without GQA two consecutive 128-token blocks of the one head. Per 128-key tile j:
+//   S_a = Q_a K_j^T      tcgen05.mma, Q_a and K_j from shared memory, S_a in TMEM
+//   softmax warpgroup a  row max (pass 1) and P_a = 2^(s - m) (pass 2) read from TMEM with
+//                        tcgen05.ld; P_a written back as bf16 over S_a's first 64 columns
+//   O_a += P_a V_j        tcgen05.mma with A = P_a read from TMEM, B = V_j (MN-major) in smem
+// The MMA warp issues S_0(j), O_1 += P_1(j-1) V(j-1), S_1(j), O_0 += P_0(j) V(j), so each
+// softmax warpgroup works while the tensor core serves the other. O_a is rescaled in TMEM
+// only when a row's running max grows by more than 2^8 (its sum l carries the same stale
+// max, so O / l is unchanged).
 //
-// Warp roles (192 threads): warps 0-3 softmax + epilogue (thread = row = TMEM lane), warp 4
-// TMA producer (Q once; K and V in 2-stage rings), warp 5 UMMA issuer and TMEM owner.
-// TMEM columns: S double buffer [0, 256), O [256, 384).
-// Shared memory: Q, 2 x K, 2 x V, P tiles of 32 KiB, all 128-byte swizzled, 1024-aligned.
+// Warps (384 threads): 0-3 softmax/epilogue of M-tile 0, 4-7 of M-tile 1 (thread = row =
+// TMEM lane), 8 scheduler + TMA producer (Q_0, Q_1 per item, each reloaded as soon as its
+// last S MMA is done; K and V in 2-stage rings), 9 UMMA issuer and TMEM owner, 10-11 idle. TMEM: S_0 [0,128), S_1 [128,256), O_0 [256,384),
+// O_1 [384,512). Shared memory: Q_0, Q_1, 2 K, 2 V tiles of 32 KiB, 128-byte swizzled.
 //
 // Rows of the last V tile past the sequence's keys are zeroed in shared memory before use
 // (P is 0 there, but 0 x NaN from a stale pool slot would still poison O).
@@ -32,31 +38,60 @@ namespace pkv {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kBM = 128;  // tile rows (G heads x 128/G tokens)
+constexpr int kBM = 128;  // rows of one M-tile
 constexpr int kBN = 128;  // keys per tile
 constexpr int kStages = 2;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kThreads = 192;
+constexpr int kThreads = 384;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr uint32_t kTileBytes = kBM * kD * 2;  // 32 KiB
 constexpr uint32_t kHalfBytes = kTileBytes / 2;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;
+constexpr unsigned kFull = 0xffffffffu;
+// Registers per thread: at launch (= 65536 / 384, what __launch_bounds__(384, 1) gives) and
+// after the split. 2 x kSoftmaxRegs + kOtherRegs must not exceed 3 x kLaunchRegs, or the
+// increase would wait forever; the launcher checks the compiled count before every launch.
+constexpr int kLaunchRegs = 168;
+constexpr int kSoftmaxRegs = 208;
+constexpr int kOtherRegs = 88;
+static_assert(2 * kSoftmaxRegs + kOtherRegs <= 3 * kLaunchRegs, "register split too large");
+
+template <int N>
+__device__ __forceinline__ void reg_alloc_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void reg_dealloc() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+struct Item {
+  int id;          // index in the work list; -1 marks the end of the work
+  int n, h;
+  int hq[2];
+  int64_t tok[2];  // first query token (within the sequence) of each M-tile
+  int64_t q0, Lq, k0, Lk;
+  int nk;          // key tiles to process
+  int last_rows;   // keys of the sequence in the last key tile
+  bool valid;      // the item has queries
+  bool bad;        // cu_seqlens / block_table inconsistent for this sequence
+};
+
+constexpr int kRing = 4;  // work items in flight between the scheduler and the other warps
 
 struct PrefillSmem {
-  uint8_t q[kTileBytes];
+  uint8_t q[2][kTileBytes];
   uint8_t k[kStages][kTileBytes];
   uint8_t v[kStages][kTileBytes];
-  uint8_t p[kTileBytes];
-  uint64_t q_full;
+  uint64_t q_full[2], q_empty[2];
   uint64_t k_full[kStages], k_empty[kStages];
   uint64_t v_full[kStages], v_empty[kStages];
-  uint64_t v_fixed;
-  uint64_t s_full[2];
-  uint64_t p_full;
-  uint64_t o_full;
+  uint64_t v_fixed[kStages];  // per stage: the next fix of a stage needs that stage released
+  uint64_t s_full[2], p_full[2], o_full[2];
+  uint64_t item_full[kRing], item_empty[kRing];
+  Item items[kRing];  // decoded once by the scheduler, read by the other warps
   uint32_t tmem_base;
 };
 
@@ -69,13 +104,103 @@ struct PrefillParams {
   int64_t num_blocks;
   int64_t total_q;
   int64_t kv_rows;
+  int32_t num_seqs;
   int32_t num_q_heads;
-  int32_t qtiles;
+  int32_t num_kv_heads;
+  int32_t qblocks;  // query blocks of one item (128 tokens with GQA pairs, 256 without)
+  int32_t items;
   float scale_log2;
   int32_t causal;
   uint16_t *out;
+  int32_t *queue;  // next item to hand out (zeroed before the launch)
   unsigned int *err;
 };
+
+
+// Item i of the walk. Items are ordered by query block, last block first, so the tiles with
+// the most keys start first; every role decodes the same sequence of items.
+template <int G>
+__device__ __forceinline__ Item decode_item(const PrefillParams &p, int i) {
+  constexpr int kPairs = G >= 2 ? G / 2 : 1;
+  Item it;
+  it.id = i;
+  const int per_qb = p.num_seqs * p.num_kv_heads * kPairs;
+  const int qb = p.qblocks - 1 - i / per_qb;
+  const int r = i % per_qb;
+  it.n = r / (p.num_kv_heads * kPairs);
+  const int hp = r % (p.num_kv_heads * kPairs);
+  it.h = hp / kPairs;
+  const int pair = hp % kPairs;
+  if (G >= 2) {
+    it.hq[0] = it.h * G + 2 * pair;
+    it.hq[1] = it.hq[0] + 1;
+    it.tok[0] = it.tok[1] = (int64_t)qb * kBM;
+  } else {
+    it.hq[0] = it.hq[1] = it.h;
+    it.tok[0] = (int64_t)qb * 2 * kBM;
+    it.tok[1] = it.tok[0] + kBM;
+  }
+  it.q0 = p.cu_q[it.n];
+  it.Lq = p.cu_q[it.n + 1] - it.q0;
+  it.k0 = p.cu_k[it.n];
+  it.Lk = p.cu_k[it.n + 1] - it.k0;
+  bool bad = it.Lq < 0 || it.Lk < 0 || it.q0 < 0 || it.q0 + it.Lq > p.total_q;
+  if (p.block_table) bad = bad || it.Lk > (int64_t)p.table_width * p.block_size;
+  else bad = bad || it.k0 < 0 || it.k0 + it.Lk > p.kv_rows;
+  it.bad = bad;
+  it.valid = !bad && it.tok[0] < it.Lq;
+  it.nk = 0;
+  it.last_rows = 0;
+  if (it.valid) {
+    int64_t kv_end = 0;
+#pragma unroll
+    for (int a = 0; a < 2; ++a) {
+      if (it.tok[a] >= it.Lq) continue;
+      const int64_t last_q = min(it.Lq, it.tok[a] + kBM) - 1;
+      const int64_t e = p.causal ? min(it.Lk, last_q + (it.Lk - it.Lq) + 1) : it.Lk;
+      kv_end = max(kv_end, e);
+    }
+    if (kv_end > 0) {
+      it.nk = (int)((kv_end + kBN - 1) / kBN);
+      it.last_rows = (int)min((int64_t)kBN, it.Lk - (int64_t)(it.nk - 1) * kBN);
+    }
+  }
+  return it;
+}
+
+// Next work item from the ring (in order). it.id < 0 at the end of the work, or when the
+// wait gave up. The caller releases the slot (item_empty) after copying the item.
+__device__ __forceinline__ Item take_item(PrefillSmem &sm, uint32_t taken, unsigned int *err) {
+  const int slot = taken % kRing;
+  Item it;
+  if (wait_parity(&sm.item_full[slot], (taken / kRing) & 1, err)) {
+    it = sm.items[slot];
+  } else {
+    it.id = -1;
+  }
+  return it;
+}
+
+// S = Q K^T for one 128 x 128 tile: 8 UMMAs of K = 16 over the two 64-column halves.
+__device__ __forceinline__ void mma_qk(uint32_t d_tmem, uint32_t q_addr, uint32_t k_addr,
+                                       uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < kD / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+    umma_bf16(d_tmem, smem_desc_sw128(q_addr + off, 16, 1024),
+              smem_desc_sw128(k_addr + off, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// O (+)= P V for one tile: P from TMEM (8 columns per 16 keys), V MN-major in smem.
+__device__ __forceinline__ void mma_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_addr,
+                                       uint32_t idesc, bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < kBN / 16; ++kk)
+    umma_bf16_tmem_a(d_tmem, p_tmem + 8 * kk,
+                     smem_desc_sw128(v_addr + kk * 16 * 128, kHalfBytes, 1024), idesc,
+                     (accumulate || kk > 0) ? 1u : 0u);
+}
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -87,44 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                    const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
-  constexpr int QT = kBM / G;  // query tokens per tile
-  const int qt = p.qtiles - 1 - (int)blockIdx.x;  // longest (most keys) tiles first
-  const int h = blockIdx.y;
-  const int n = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-  const int64_t q0 = p.cu_q[n], Lq = p.cu_q[n + 1] - q0;
-  const int64_t k0 = p.cu_k[n], Lk = p.cu_k[n + 1] - k0;
-  bool bad = Lq < 0 || Lk < 0 || q0 < 0 || q0 + Lq > p.total_q;
-  if (p.block_table) bad = bad || Lk > (int64_t)p.table_width * p.block_size;
-  else bad = bad || k0 < 0 || k0 + Lk > p.kv_rows;
-  if (bad) {
-    if (tid == 0 && qt == p.qtiles - 1 && h == 0) record_error(p.err, 8u /* SEQLEN_RANGE */);
-    return;
-  }
-  if (tid == 0 && qt == p.qtiles - 1 && h == 0 && Lq > (int64_t)p.qtiles * QT)
-    record_error(p.err, 8u);
-  const int64_t qbeg = (int64_t)qt * QT;
-  if (qbeg >= Lq) return;
-  const int hq0 = h * G;
-  const int64_t qlast = min(Lq, qbeg + QT) - 1;
-  const int64_t kv_end = p.causal ? min(Lk, qlast + (Lk - Lq) + 1) : Lk;
-  const int nk = kv_end > 0 ? (int)((kv_end + kBN - 1) / kBN) : 0;
-
-  if (nk == 0) {  // no row of this tile sees a key: zeros
-    for (int idx = tid; idx < kBM * 16; idx += kThreads) {
-      const int r = idx >> 4, c = idx & 15;
-      const int64_t qi = qbeg + r % QT;
-      if (qi < Lq)
-        reinterpret_cast<uint4 *>(p.out + ((q0 + qi) * p.num_q_heads + hq0 + r / QT) * kD)[c] =
-            make_uint4(0, 0, 0, 0);
-    }
-    return;
-  }
-  // rows of the last key tile that hold keys of this sequence
-  const int last_rows = (int)min((int64_t)kBN, Lk - (int64_t)(nk - 1) * kBN);
-  const bool fix_v = last_rows < kBN;
-
   extern __shared__ uint8_t smem_raw[];
   PrefillSmem &sm = *reinterpret_cast<PrefillSmem *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -132,17 +220,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   // an earlier wait gave up somewhere: return before allocating anything (uniform)
   if (__syncthreads_or(tid == 0 && aborted(p.err))) return;
   if (tid == 0) {
-    mbar_init(&sm.q_full, 1);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&sm.q_full[a], 1);
+      mbar_init(&sm.q_empty[a], 1);
+    }
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(&sm.item_full[i], 1);
+      mbar_init(&sm.item_empty[i], 1 + 8);  // the MMA thread and the 8 softmax warps
+    }
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&sm.k_full[i], 1);
       mbar_init(&sm.k_empty[i], 1);
       mbar_init(&sm.v_full[i], 1);
       mbar_init(&sm.v_empty[i], 1);
-      mbar_init(&sm.s_full[i], 1);
+      mbar_init(&sm.v_fixed[i], 1);
     }
-    mbar_init(&sm.v_fixed, 1);
-    mbar_init(&sm.p_full, 4);
-    mbar_init(&sm.o_full, 1);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&sm.s_full[a], 1);
+      mbar_init(&sm.p_full[a], 4);
+      mbar_init(&sm.o_full[a], 1);
+    }
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -154,227 +251,335 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = sm.tmem_base;
 
+  // Consumers take item ids from the ring in order; every slot is released by the MMA thread
+  // and the 8 softmax warps. Returns -1 at the end of the work (or when a wait gave up).
+
+  // Register split (launch: kLaunchRegs x 384 threads): the two softmax warpgroups hold a
+  // whole 128-column S row per thread; warpgroup 2 only schedules, loads and issues MMAs.
+  // Each warpgroup executes one setmaxnreg, and the roles are nested under it.
+  if (warp >= 8) {
+  reg_dealloc<kOtherRegs>();
   if (warp == kProducerWarp) {
-    // ------------------------------------------------------------------ TMA producer
-    int issued = 0;
-    bool ok = true;
+    // ------------------------------------------------------------- scheduler + TMA producer
+    uint64_t pol_q = 0, pol_kv = 0;
     if (lane == 0) {
       prefetch_tensormap(&qmap);
       prefetch_tensormap(&kmap);
       prefetch_tensormap(&vmap);
-      const uint64_t pol_q = policy_evict_first();
-      const uint64_t pol_kv = policy_evict_last();
-      mbar_arrive_expect_tx(&sm.q_full, kTileBytes);
-      for (int g = 0; g < G; ++g)
-        for (int hf = 0; hf < 2; ++hf)
-          tma_load_3d(sm.q + hf * kHalfBytes + g * QT * 128, &qmap, &sm.q_full, 0,
-                      (int32_t)(q0 + qbeg), 2 * (hq0 + g) + hf, pol_q);
-      for (int j = 0; j < nk; ++j) {
-        const int st = j % kStages;
-        int32_t row;
-        if (p.block_table) {
-          const int64_t key = (int64_t)j * kBN;
-          const int64_t blk = p.block_table[(int64_t)n * p.table_width + key / p.block_size];
-          if (blk < 0 || blk >= p.num_blocks) {
-            record_error(p.err, 2u /* BLOCK_RANGE */);
-            row = -2 * kBN;  // wholly outside the pool: TMA fills zeros
-          } else {
-            row = (int32_t)(blk * p.block_size + key % p.block_size);
-          }
-        } else {
-          row = (int32_t)(k0 + (int64_t)j * kBN);
-        }
-        if (j >= kStages && !wait_parity(&sm.k_empty[st], ((j / kStages) - 1) & 1, p.err)) {
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
-        tma_load_3d(sm.k[st], &kmap, &sm.k_full[st], 0, row, 2 * h, pol_kv);
-        if (j >= kStages && !wait_parity(&sm.v_empty[st], ((j / kStages) - 1) & 1, p.err)) {
-          ok = false;
-          issued = -(j + 1);  // K_j issued, V_j not
-          break;
-        }
-        mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
-        tma_load_3d(sm.v[st], &vmap, &sm.v_full[st], 0, row, 2 * h, pol_kv);
-        issued = j + 1;
-      }
-      if (!ok) record_error(p.err, 16u /* TIMEOUT */);
+      pol_q = policy_evict_first();
+      pol_kv = policy_evict_last();
     }
-    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    if (ok && fix_v) {
-      const int j = nk - 1, st = j % kStages;
-      const bool landed = wait_parity(&sm.v_full[st], (j / kStages) & 1, p.err);
-      if (landed) {
-        uint8_t *vt = sm.v[st];
-        for (int idx = lane; idx < (kBN - last_rows) * 16; idx += 32) {
-          const int r = last_rows + (idx >> 4), c = idx & 15;
-          *reinterpret_cast<uint4 *>(vt + (c >> 3) * kHalfBytes + r * 128 + (c & 7) * 16) =
-              make_uint4(0, 0, 0, 0);
+    uint32_t pushed = 0, q_loads = 0, g = 0;
+    int last_k = -1, last_v = -1;
+    bool ok = true;
+    while (ok) {
+      // take the next item that has queries; -1 when the queue is exhausted
+      int i = -1;
+      if (lane == 0) {
+        Item d;
+        d.id = -1;
+        while (true) {
+          i = atomicAdd(p.queue, 1);
+          if (i >= p.items) break;
+          d = decode_item<G>(p, i);
+          if (d.bad) record_error(p.err, 8u /* SEQLEN_RANGE */);
+          if (d.valid) break;
         }
-        fence_async_shared();
-      } else if (lane == 0) {
-        record_error(p.err, 16u);
+        if (i >= p.items) {
+          i = -1;
+          d.id = -1;
+        }
+        const int slot = pushed % kRing;
+        if (pushed >= kRing)
+          ok = wait_parity(&sm.item_empty[slot], ((pushed / kRing) - 1) & 1, p.err);
+        if (ok) {
+          sm.items[slot] = d;
+          mbar_arrive(&sm.item_full[slot]);  // release: the item is visible to the waiters
+        }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.v_fixed);
+      ++pushed;
+      ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+      i = __shfl_sync(kFull, i, 0);
+      if (!ok || i < 0) break;
+      __syncwarp();  // lane 0 wrote the slot
+      const Item it = sm.items[(pushed - 1) % kRing];
+      if (it.nk == 0) continue;  // no key visible: the softmax warps write zeros
+      if (lane == 0) {
+#pragma unroll
+        for (int a = 0; a < 2; ++a) {
+          if (q_loads > 0) ok = ok && wait_parity(&sm.q_empty[a], (q_loads - 1) & 1, p.err);
+          if (ok) {
+            mbar_arrive_expect_tx(&sm.q_full[a], kTileBytes);
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf)
+              tma_load_3d(sm.q[a] + hf * kHalfBytes, &qmap, &sm.q_full[a], 0,
+                          (int32_t)(it.q0 + it.tok[a]), 2 * it.hq[a] + hf, pol_q);
+          }
+        }
+      }
+      ++q_loads;
+      ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+      for (int j = 0; j < it.nk && ok; ++j, ++g) {
+        const int st = g % kStages;
+        if (lane == 0) {
+          int32_t row;
+          if (p.block_table) {
+            const int64_t key = (int64_t)j * kBN;
+            const int64_t blk = p.block_table[(int64_t)it.n * p.table_width + key / p.block_size];
+            if (blk < 0 || blk >= p.num_blocks) {
+              record_error(p.err, 2u /* BLOCK_RANGE */);
+              row = -2 * kBN;  // wholly outside the pool: TMA fills zeros
+            } else {
+              row = (int32_t)(blk * p.block_size + key % p.block_size);
+            }
+          } else {
+            row = (int32_t)(it.k0 + (int64_t)j * kBN);
+          }
+          if (g >= kStages) ok = wait_parity(&sm.k_empty[st], ((g / kStages) - 1) & 1, p.err);
+          if (ok) {
+            mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
+            tma_load_3d(sm.k[st], &kmap, &sm.k_full[st], 0, row, 2 * it.h, pol_kv);
+            last_k = (int)g;
+          }
+          if (ok && g >= kStages)
+            ok = wait_parity(&sm.v_empty[st], ((g / kStages) - 1) & 1, p.err);
+          if (ok) {
+            mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
+            tma_load_3d(sm.v[st], &vmap, &sm.v_full[st], 0, row, 2 * it.h, pol_kv);
+            last_v = (int)g;
+          }
+        }
+        ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+        if (ok && j == it.nk - 1 && it.last_rows < kBN) {
+          // zero the rows past the sequence's keys before the MMA reads this V tile
+          ok = __all_sync(kFull, wait_parity(&sm.v_full[st], (g / kStages) & 1, p.err));
+          if (ok) {
+            uint8_t *vt = sm.v[st];
+            for (int idx = lane; idx < (kBN - it.last_rows) * 16; idx += 32) {
+              const int r = it.last_rows + (idx >> 4), c = idx & 15;
+              *reinterpret_cast<uint4 *>(vt + (c >> 3) * kHalfBytes + r * 128 + (c & 7) * 16) =
+                  make_uint4(0, 0, 0, 0);
+            }
+            fence_async_shared();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.v_fixed[st]);
+          }
+        }
+      }
     }
     if (lane == 0) {  // keep the CTA alive until every copy issued has landed
-      const int kdone = issued >= 0 ? issued : -issued;
-      const int vdone = issued >= 0 ? issued : -issued - 1;
-      bool drained = wait_parity(&sm.q_full, 0, p.err);
-      for (int j = max(0, kdone - kStages); drained && j < kdone; ++j)
-        drained = wait_parity(&sm.k_full[j % kStages], (j / kStages) & 1, p.err);
-      for (int j = max(0, vdone - kStages); drained && j < vdone; ++j)
-        drained = wait_parity(&sm.v_full[j % kStages], (j / kStages) & 1, p.err);
-      if (!drained) record_error(p.err, 16u);
+      bool drained = true;
+      for (int a = 0; a < 2 && q_loads > 0; ++a)
+        drained = drained && wait_parity(&sm.q_full[a], (q_loads - 1) & 1, p.err);
+      for (int t = max(0, last_k - kStages + 1); drained && t <= last_k; ++t)
+        drained = wait_parity(&sm.k_full[t % kStages], (t / kStages) & 1, p.err);
+      for (int t = max(0, last_v - kStages + 1); drained && t <= last_v; ++t)
+        drained = wait_parity(&sm.v_full[t % kStages], (t / kStages) & 1, p.err);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ UMMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16_f32(kBM, kBN, 0, 0);  // Q (K-major) x K (K-major)
-      constexpr uint32_t kIdO = idesc_bf16_f32(kBM, kD, 0, 1);   // P (K-major) x V (MN-major)
-      const uint32_t qa = smem_addr(sm.q), pa = smem_addr(sm.p);
-      bool ok = wait_parity(&sm.q_full, 0, p.err);
-      auto issue_pv = [&](int i) {
-        if (!ok) return;
-        const int st = i % kStages;
-        ok = wait_parity(&sm.p_full, i & 1, p.err) &&
-             ((i == nk - 1 && fix_v) ? wait_parity(&sm.v_fixed, 0, p.err)
-                                     : wait_parity(&sm.v_full[st], (i / kStages) & 1, p.err));
-        if (!ok) return;
-        tc_fence_after_sync();
-        const uint32_t va = smem_addr(sm.v[st]);
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint64_t ad = smem_desc_sw128(pa + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(va + kk * 16 * 128, kHalfBytes, 1024);
-          umma_bf16(tmem + kTmemO, ad, bd, kIdO, (i > 0 || kk > 0) ? 1u : 0u);
+      constexpr uint32_t kIdO = idesc_bf16_f32(kBM, kD, 0, 1);   // P (TMEM) x V (MN-major)
+      const uint32_t qa0 = smem_addr(sm.q[0]), qa1 = smem_addr(sm.q[1]);
+      const uint32_t ka0 = smem_addr(sm.k[0]), ka1 = smem_addr(sm.k[1]);
+      const uint32_t va0 = smem_addr(sm.v[0]), va1 = smem_addr(sm.v[1]);
+      uint32_t taken = 0, q_loads = 0, g = 0, fix0 = 0, fix1 = 0;
+      bool ok = true;
+      while (ok) {
+        const Item it = take_item(sm, taken, p.err);
+        mbar_arrive(&sm.item_empty[taken % kRing]);
+        ++taken;
+        if (it.id < 0) break;
+        if (it.nk == 0) continue;
+        const int nk = it.nk;
+        const bool fix_v = it.last_rows < kBN;
+        for (int j = 0; j < nk; ++j, ++g) {
+          const uint32_t st = g & 1;
+          const uint32_t ka = st ? ka1 : ka0;
+          ok = wait_parity(&sm.k_full[st], (g >> 1) & 1, p.err);
+          if (!ok) break;
+          tc_fence_after_sync();
+          // S_0(j)
+          if (j == 0) {
+            ok = wait_parity(&sm.q_full[0], q_loads & 1, p.err);
+            if (!ok) break;
+            tc_fence_after_sync();
+          }
+          mma_qk(tmem, qa0, ka, kIdS);
+          umma_commit(&sm.s_full[0]);
+          if (j == nk - 1) umma_commit(&sm.q_empty[0]);
+          // O_1 += P_1(j-1) V(j-1)  (never the last tile here)
+          if (j > 0) {
+            const uint32_t gp = g - 1, sp = gp & 1;
+            ok = wait_parity(&sm.p_full[1], gp & 1, p.err) &&
+                 wait_parity(&sm.v_full[sp], (gp >> 1) & 1, p.err);
+            if (!ok) break;
+            tc_fence_after_sync();
+            mma_pv(tmem + 384, tmem + 128, sp ? va1 : va0, kIdO, j - 1 > 0);
+            umma_commit(&sm.o_full[1]);
+            umma_commit(&sm.v_empty[sp]);
+          }
+          // S_1(j)
+          if (j == 0) {
+            ok = wait_parity(&sm.q_full[1], q_loads & 1, p.err);
+            if (!ok) break;
+            tc_fence_after_sync();
+          }
+          mma_qk(tmem + 128, qa1, ka, kIdS);
+          umma_commit(&sm.s_full[1]);
+          if (j == nk - 1) umma_commit(&sm.q_empty[1]);
+          umma_commit(&sm.k_empty[st]);
+          // O_0 += P_0(j) V(j)
+          ok = wait_parity(&sm.p_full[0], g & 1, p.err) &&
+               ((j == nk - 1 && fix_v)
+                    ? wait_parity(&sm.v_fixed[st], (st ? fix1 : fix0) & 1, p.err)
+                    : wait_parity(&sm.v_full[st], (g >> 1) & 1, p.err));
+          if (!ok) break;
+          tc_fence_after_sync();
+          mma_pv(tmem + 256, tmem, st ? va1 : va0, kIdO, j > 0);
+          umma_commit(&sm.o_full[0]);
         }
-        umma_commit(&sm.v_empty[st]);
-        umma_commit(&sm.o_full);
-      };
-      for (int j = 0; j < nk && ok; ++j) {
-        const int st = j % kStages;
-        ok = wait_parity(&sm.k_full[st], (j / kStages) & 1, p.err);
+        if (!ok) break;
+        {  // O_1 += P_1(last) V(last)
+          const uint32_t gp = g - 1, sp = gp & 1;
+          ok = wait_parity(&sm.p_full[1], gp & 1, p.err) &&
+               (fix_v ? wait_parity(&sm.v_fixed[sp], (sp ? fix1 : fix0) & 1, p.err)
+                      : wait_parity(&sm.v_full[sp], (gp >> 1) & 1, p.err));
+          if (!ok) break;
+          tc_fence_after_sync();
+          mma_pv(tmem + 384, tmem + 128, sp ? va1 : va0, kIdO, nk > 1);
+          umma_commit(&sm.o_full[1]);
+          umma_commit(&sm.v_empty[sp]);
+          if (fix_v) {
+            if (sp) ++fix1;
+            else ++fix0;
+          }
+        }
+        ++q_loads;
+      }
+      // every UMMA must be complete before the tensor memory is released
+      if (ok && g > 0) wait_parity(&sm.o_full[1], (g - 1) & 1, p.err);
+    }
+  }
+  } else {
+    reg_alloc_inc<kSoftmaxRegs>();
+    // ------------------------------------------------------------------ softmax warps
+    const int a = warp >> 2;        // M-tile
+    const int r = tid & (kBM - 1);  // row == TMEM lane
+    const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t s_col = 128 * a, o_col = 256 + 128 * a;
+    const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
+    uint32_t taken = 0, g = 0;
+    bool ok = true;
+    while (ok) {
+      Item it = take_item(sm, taken, p.err);
+      it.id = __shfl_sync(kFull, it.id, 0);  // warp-uniform end / give-up decision
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.item_empty[taken % kRing]);
+      ++taken;
+      if (it.id < 0) break;
+      const int64_t qi = it.tok[a] + r;
+      const bool row_valid = qi < it.Lq;
+      uint4 *dst = reinterpret_cast<uint4 *>(
+          p.out + ((it.q0 + qi) * p.num_q_heads + it.hq[a]) * kD);
+      if (it.nk == 0) {  // no key is visible to any row: zeros
+        if (row_valid)
+          for (int c = 0; c < 16; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+        continue;
+      }
+      int64_t lim = !row_valid ? -1 : (p.causal ? qi + (it.Lk - it.Lq) : it.Lk - 1);
+      if (lim > it.Lk - 1) lim = it.Lk - 1;
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int j = 0; j < it.nk; ++j, ++g) {
+        // warp-uniform results: the TMEM loads and stores below are .sync.aligned
+        ok = __all_sync(kFull, wait_parity(&sm.s_full[a], g & 1, p.err));
         if (!ok) break;
         tc_fence_after_sync();
-        const uint32_t ka = smem_addr(sm.k[st]);
-        const uint32_t d = tmem + (uint32_t)(j & 1) * kBN;
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          umma_bf16(d, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
-                    kIdS, kk > 0 ? 1u : 0u);
-        }
-        umma_commit(&sm.k_empty[st]);
-        umma_commit(&sm.s_full[j & 1]);
-        if (j >= 1) issue_pv(j - 1);
-      }
-      issue_pv(nk - 1);
-      // every UMMA must be complete before the tensor memory is released
-      if (!ok || !wait_parity(&sm.o_full, (nk - 1) & 1, p.err)) record_error(p.err, 16u);
-    }
-  } else {
-    // ------------------------------------------------------------------ softmax warps
-    const int r = tid;  // tile row == TMEM lane
-    const int g = r / QT;
-    const int64_t qi = qbeg + r % QT;
-    const bool row_valid = qi < Lq;
-    int64_t lim = !row_valid ? -1 : (p.causal ? qi + (Lk - Lq) : Lk - 1);
-    if (lim > Lk - 1) lim = Lk - 1;
-    const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-    const int sw = r & 7;
-    float m_run = -INFINITY, l_run = 0.f;
-    bool ok = true;
-    for (int j = 0; j < nk; ++j) {
-      // warp-uniform results: the TMEM loads and stores below are .sync.aligned
-      if (!__all_sync(0xffffffffu, wait_parity(&sm.s_full[j & 1], (j >> 1) & 1, p.err))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after_sync();
-      uint32_t s[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(lane_addr + (uint32_t)(j & 1) * kBN + c * 32, s[c]);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld_wait(s[c]);
+        const int64_t rel = lim - (int64_t)j * kBN;  // last visible column of this tile
+        const int lim_rel = (int)(rel < -1 ? -1 : (rel > kBN ? kBN : rel));
 
-      const int64_t kbase = (int64_t)j * kBN;
-      const bool full = kbase + kBN - 1 <= lim;
-      float mx = -INFINITY;
+        // the whole S row in registers: one TMEM round trip per tile
+        uint32_t x[4][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 4; ++c) tmem_ld32(lane_addr + s_col + 32 * c, x[c]);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float x = __uint_as_float(s[c][e]) * p.scale_log2;
-          if (!full && kbase + c * 32 + e > lim) x = -INFINITY;
-          s[c][e] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
+        for (int c = 0; c < 4; ++c) tmem_ld_wait(x[c]);
+        if (lim_rel < kBN - 1) {  // diagonal or last tile: columns past lim_rel are -inf
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (32 * c + e > lim_rel) x[c][e] = __float_as_uint(-INFINITY);
         }
-      const float m_new = fmaxf(m_run, mx);
-      const bool rescale = m_new > m_run + kRescaleLog2;
-      float alpha = 1.f;
-      if (rescale) {
-        alpha = fast_exp2(m_run - m_new);
-        m_run = m_new;
-        l_run *= alpha;
-      }
-      const float m_use = m_run == -INFINITY ? 0.f : m_run;
-      uint32_t pk[64];
-      float rowsum = 0.f;
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float p0 = fast_exp2(__uint_as_float(s[c][2 * e]) - m_use);
-          const float p1 = fast_exp2(__uint_as_float(s[c][2 * e + 1]) - m_use);
-          rowsum += p0 + p1;
-          pk[c * 16 + e] = pack_bf16(p0, p1);
-        }
-      l_run += rowsum;
-
-      // P_{j-1} V_{j-1} must be done before P is overwritten and O is rescaled
-      if (j >= 1) {
-        if (!__all_sync(0xffffffffu, wait_parity(&sm.o_full, (j - 1) & 1, p.err))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-      }
-#pragma unroll
-      for (int c16 = 0; c16 < 16; ++c16) {
-        uint8_t *dst = sm.p + (c16 >> 3) * kHalfBytes + r * 128 + (((c16 & 7) ^ sw) << 4);
-        *reinterpret_cast<uint4 *>(dst) =
-            make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
-      }
-      if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
+        float mx[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          uint32_t o[32];
-          tmem_ld32(lane_addr + kTmemO + c * 32, o);
-          tmem_ld_wait(o);
+          mx[c] = -INFINITY;
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(lane_addr + kTmemO + c * 32, o);
+          for (int e = 0; e < 32; e += 2)
+            mx[c] = fmax3(mx[c], __uint_as_float(x[c][e]), __uint_as_float(x[c][e + 1]));
+        }
+        const float m_tile = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * p.scale_log2;
+        const float m_new = fmaxf(m_run, m_tile);
+        const bool rescale = m_new > m_run + kRescaleLog2;
+        float alpha = 1.f;
+        if (rescale) {
+          alpha = fast_exp2(m_run - m_new);
+          m_run = m_new;
+          l_run *= alpha;
+        }
+        const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
+
+        // O_a holds the tiles before this one: rescale it (never on the first tile)
+        if (j > 0 && __any_sync(kFull, rescale)) {
+          ok = __all_sync(kFull, wait_parity(&sm.o_full[a], (g - 1) & 1, p.err));
+          if (!ok) break;
+          tc_fence_after_sync();
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            tmem_ld32(lane_addr + o_col + 32 * c, o);
+            tmem_ld_wait(o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(lane_addr + o_col + 32 * c, o);
+          }
+        }
+
+        // P = 2^(s * scale_log2 - m) as bf16 pairs over the first 64 columns of S
+        const float2 nm2 = make_float2(neg_m, neg_m);
+        float2 rs0 = make_float2(0.f, 0.f), rs1 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float2 t = ffma2(make_float2(__uint_as_float(x[c][2 * e]),
+                                               __uint_as_float(x[c][2 * e + 1])), sl2, nm2);
+            const float2 pe = make_float2(fast_exp2(t.x), fast_exp2(t.y));
+            if (e & 1) rs1 = fadd2(rs1, pe);
+            else rs0 = fadd2(rs0, pe);
+            pk[e] = pack_bf16(pe.x, pe.y);
+          }
+          tmem_st16(lane_addr + s_col + 16 * c, pk);
         }
         tmem_st_wait();
+        l_run += (rs0.x + rs0.y) + (rs1.x + rs1.y);
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.p_full[a]);
       }
-      fence_async_shared();
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.p_full);
-    }
-    // ---- epilogue: O / l -> bf16 rows
-    if (ok) ok = __all_sync(0xffffffffu, wait_parity(&sm.o_full, (nk - 1) & 1, p.err));
-    if (ok) {
+      if (!ok) break;
+      // ---- epilogue: O / l -> bf16 rows
+      ok = __all_sync(kFull, wait_parity(&sm.o_full[a], (g - 1) & 1, p.err));
+      if (!ok) break;
       tc_fence_after_sync();
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((q0 + qi) * p.num_q_heads + hq0 + g) * kD);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t o[32];
-        tmem_ld32(lane_addr + kTmemO + c * 32, o);
+        tmem_ld32(lane_addr + o_col + 32 * c, o);
         tmem_ld_wait(o);
         if (row_valid) {
 #pragma unroll
@@ -400,12 +605,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int G>
-cudaError_t launch_g(const PrefillArgs &a, const PrefillParams &prm, cudaStream_t stream) {
-  constexpr int QT = kBM / G;
+cudaError_t launch_g(const PrefillArgs &a, PrefillParams prm, int num_sms, cudaStream_t stream) {
+  constexpr int kPairs = G >= 2 ? G / 2 : 1;
+  constexpr int kTokensPerItem = G >= 2 ? kBM : 2 * kBM;
   CUtensorMap qm, km, vm;
   const uint64_t qdims[3] = {64, (uint64_t)a.total_q, (uint64_t)a.num_q_heads * 2};
   const uint64_t qstr[2] = {(uint64_t)a.q_tok_stride * 2, 128};
-  const uint32_t qbox[3] = {64, (uint32_t)QT, 1};
+  const uint32_t qbox[3] = {64, (uint32_t)kBM, 1};
   const uint64_t kvdims[3] = {64, (uint64_t)(a.kv_rows > 0 ? a.kv_rows : 1),
                               (uint64_t)a.num_kv_heads * 2};
   const uint64_t kvstr[2] = {(uint64_t)a.kv_tok_stride * 2, 128};
@@ -425,15 +631,28 @@ cudaError_t launch_g(const PrefillArgs &a, const PrefillParams &prm, cudaStream_
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<G>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    // The register split inside the kernel draws on the registers the CTA is launched with;
+    // never launch a build whose count cannot cover it (the increase would never return).
+    cudaFuncAttributes fa{};
+    cudaError_t e = cudaFuncGetAttributes(&fa, prefill_kernel<G>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs * kThreads < (2 * kSoftmaxRegs + kOtherRegs) * 128)
+      return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(prefill_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  PrefillParams p2 = prm;
-  p2.qtiles = (a.max_seqlen_q + QT - 1) / QT;
-  const dim3 grid((unsigned)p2.qtiles, (unsigned)a.num_kv_heads, (unsigned)a.num_seqs);
-  prefill_kernel<G><<<grid, kThreads, smem, stream>>>(qm, km, vm, p2);
+  prm.qblocks = (a.max_seqlen_q + kTokensPerItem - 1) / kTokensPerItem;
+  prm.queue = static_cast<int32_t *>(a.workspace);
+  const int64_t items = (int64_t)prm.qblocks * a.num_seqs * a.num_kv_heads * kPairs;
+  if (items <= 0) return cudaSuccess;
+  if (items > INT32_MAX) return cudaErrorInvalidValue;
+  prm.items = (int32_t)items;
+  const unsigned grid = (unsigned)(items < num_sms ? items : num_sms);
+  cudaError_t e = cudaMemsetAsync(a.workspace, 0, kPrefillWorkspaceBytes, stream);
+  if (e != cudaSuccess) return e;
+  prefill_kernel<G><<<grid, kThreads, smem, stream>>>(qm, km, vm, prm);
   return cudaGetLastError();
 }
 
@@ -444,7 +663,6 @@ bool prefill_group_supported(int group) {
 }
 
 cudaError_t launch_varlen_prefill(const PrefillArgs &a, int num_sms, cudaStream_t stream) {
-  (void)num_sms;
   PrefillParams prm{};
   prm.cu_q = a.cu_seqlens_q;
   prm.cu_k = a.cu_seqlens_k;
@@ -454,16 +672,18 @@ cudaError_t launch_varlen_prefill(const PrefillArgs &a, int num_sms, cudaStream_
   prm.num_blocks = a.num_blocks;
   prm.total_q = a.total_q;
   prm.kv_rows = a.kv_rows;
+  prm.num_seqs = a.num_seqs;
   prm.num_q_heads = a.num_q_heads;
+  prm.num_kv_heads = a.num_kv_heads;
   prm.scale_log2 = a.scale * kLog2e;
   prm.causal = a.causal;
   prm.out = static_cast<uint16_t *>(a.out);
   prm.err = a.err;
   switch (a.num_q_heads / a.num_kv_heads) {
-    case 1: return launch_g<1>(a, prm, stream);
-    case 2: return launch_g<2>(a, prm, stream);
-    case 4: return launch_g<4>(a, prm, stream);
-    case 8: return launch_g<8>(a, prm, stream);
+    case 1: return launch_g<1>(a, prm, num_sms, stream);
+    case 2: return launch_g<2>(a, prm, num_sms, stream);
+    case 4: return launch_g<4>(a, prm, num_sms, stream);
+    case 8: return launch_g<8>(a, prm, num_sms, stream);
     default: return cudaErrorNotSupported;
   }
 }

@@ -70,12 +70,12 @@ def test_decode_argument_checks():
 def _prefill(**kw):
     a = dict(q=FAKE, qs=2048, tq=100, k=FAKE, v=FAKE, kvs=1024, tk=100, cq=FAKE, ck=FAKE, N=2,
              mq=64, mk=64, bt=None, W=0, bs=0, nb=0, hq=16, hkv=8, d=128, scale=0.088, causal=1,
-             out=FAKE)
+             ws=FAKE, wsb=16, out=FAKE)
     a.update(kw)
     return L.pkv_varlen_prefill_attn(a["q"], a["qs"], a["tq"], a["k"], a["v"], a["kvs"], a["tk"],
                                      a["cq"], a["ck"], a["N"], a["mq"], a["mk"], a["bt"], a["W"],
                                      a["bs"], a["nb"], a["hq"], a["hkv"], a["d"], a["scale"],
-                                     a["causal"], None, 0, a["out"], None)
+                                     a["causal"], a["ws"], a["wsb"], a["out"], None)
 
 
 def test_prefill_argument_checks():
@@ -90,13 +90,16 @@ def test_prefill_argument_checks():
     assert _prefill(bt=FAKE, W=4, bs=128, nb=4) == pkv.ERR_UNSUPPORTED
     assert _prefill(bt=FAKE, W=4, bs=256, nb=4, kvs=2048) == pkv.ERR_UNSUPPORTED
     assert _prefill(qs=2052) == pkv.ERR_UNSUPPORTED                # stride not 16-byte multiple
+    assert _prefill(ws=None) == pkv.ERR_WORKSPACE
+    assert _prefill(wsb=8) == pkv.ERR_WORKSPACE
 
 
 def test_workspace_query_without_device_is_zero_or_sized():
     n = L.pkv_decode_workspace_bytes(4, 16, 8, 128, 300, 0)
     assert n == 0 or n >= 4 * 16 * 2 * 129 * 4
     assert L.pkv_decode_workspace_bytes(4, 16, 8, 64, 300, 0) == 0
-    assert L.pkv_prefill_workspace_bytes(4, 100, 16, 128) == 0
+    assert L.pkv_prefill_workspace_bytes(4, 100, 16, 128) == 16
+    assert L.pkv_prefill_workspace_bytes(-1, 100, 16, 128) == 0
 
 
 def test_product_path_has_no_oracle_import():
