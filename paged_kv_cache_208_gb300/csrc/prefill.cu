@@ -23,8 +23,9 @@
 //
 // Warps (384 threads): 0-3 softmax/epilogue of M-tile 0, 4-7 of M-tile 1 (thread = row =
 // TMEM lane), 8 scheduler + TMA producer (Q_0, Q_1 per item, each reloaded as soon as its
-// last S MMA is done; K and V in 2-stage rings), 9 UMMA issuer and TMEM owner, 10-11 idle. TMEM: S_0 [0,128), S_1 [128,256), O_0 [256,384),
-// O_1 [384,512). Shared memory: Q_0, Q_1, 2 K, 2 V tiles of 32 KiB, 128-byte swizzled.
+// last S MMA is done; K and V tiles through one 5-slot ring), 9 UMMA issuer and TMEM
+// owner, 10-11 idle. TMEM: S_0 [0,128), S_1 [128,256), O_0 [256,384),
+// O_1 [384,512). Shared memory: Q_0, Q_1 and 5 K/V slots of 32 KiB, 128-byte swizzled.
 //
 // Rows of the last V tile past the sequence's keys are zeroed in shared memory before use
 // (P is 0 there, but 0 x NaN from a stale pool slot would still poison O).
@@ -40,7 +41,7 @@ namespace {
 constexpr int kD = 128;
 constexpr int kBM = 128;  // rows of one M-tile
 constexpr int kBN = 128;  // keys per tile
-constexpr int kStages = 2;
+constexpr int kSlots = 5;  // K/V ring: K(j) is load 2j and V(j) load 2j + 1, slot = load % 5
 constexpr int kThreads = 384;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
@@ -83,12 +84,10 @@ constexpr int kRing = 4;  // work items in flight between the scheduler and the 
 
 struct PrefillSmem {
   uint8_t q[2][kTileBytes];
-  uint8_t k[kStages][kTileBytes];
-  uint8_t v[kStages][kTileBytes];
+  uint8_t kv[kSlots][kTileBytes];
   uint64_t q_full[2], q_empty[2];
-  uint64_t k_full[kStages], k_empty[kStages];
-  uint64_t v_full[kStages], v_empty[kStages];
-  uint64_t v_fixed[kStages];  // per stage: the next fix of a stage needs that stage released
+  uint64_t kv_full[kSlots], kv_empty[kSlots];
+  uint64_t v_fixed[kSlots];  // per slot: the next fix of a slot needs that slot released
   uint64_t s_full[2], p_full[2], o_full[2];
   uint64_t item_full[kRing], item_empty[kRing];
   Item items[kRing];  // decoded once by the scheduler, read by the other warps
@@ -228,11 +227,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.item_full[i], 1);
       mbar_init(&sm.item_empty[i], 1 + 8);  // the MMA thread and the 8 softmax warps
     }
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(&sm.k_full[i], 1);
-      mbar_init(&sm.k_empty[i], 1);
-      mbar_init(&sm.v_full[i], 1);
-      mbar_init(&sm.v_empty[i], 1);
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(&sm.kv_full[i], 1);
+      mbar_init(&sm.kv_empty[i], 1);
       mbar_init(&sm.v_fixed[i], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -270,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       pol_kv = policy_evict_last();
     }
     uint32_t pushed = 0, q_loads = 0, g = 0;
-    int last_k = -1, last_v = -1;
+    int last_load = -1;
     bool ok = true;
     while (ok) {
       // take the next item that has queries; -1 when the queue is exhausted
@@ -320,7 +317,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++q_loads;
       ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
       for (int j = 0; j < it.nk && ok; ++j, ++g) {
-        const int st = g % kStages;
+        const uint32_t nk_load = 2 * g, nv_load = 2 * g + 1;
+        const int ks = nk_load % kSlots, vs = nv_load % kSlots;
         if (lane == 0) {
           int32_t row;
           if (p.block_table) {
@@ -335,26 +333,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             row = (int32_t)(it.k0 + (int64_t)j * kBN);
           }
-          if (g >= kStages) ok = wait_parity(&sm.k_empty[st], ((g / kStages) - 1) & 1, p.err);
+          if (nk_load >= kSlots)
+            ok = wait_parity(&sm.kv_empty[ks], ((nk_load / kSlots) - 1) & 1, p.err);
           if (ok) {
-            mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
-            tma_load_3d(sm.k[st], &kmap, &sm.k_full[st], 0, row, 2 * it.h, pol_kv);
-            last_k = (int)g;
+            mbar_arrive_expect_tx(&sm.kv_full[ks], kTileBytes);
+            tma_load_3d(sm.kv[ks], &kmap, &sm.kv_full[ks], 0, row, 2 * it.h, pol_kv);
+            last_load = (int)nk_load;
           }
-          if (ok && g >= kStages)
-            ok = wait_parity(&sm.v_empty[st], ((g / kStages) - 1) & 1, p.err);
+          if (ok && nv_load >= kSlots)
+            ok = wait_parity(&sm.kv_empty[vs], ((nv_load / kSlots) - 1) & 1, p.err);
           if (ok) {
-            mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
-            tma_load_3d(sm.v[st], &vmap, &sm.v_full[st], 0, row, 2 * it.h, pol_kv);
-            last_v = (int)g;
+            mbar_arrive_expect_tx(&sm.kv_full[vs], kTileBytes);
+            tma_load_3d(sm.kv[vs], &vmap, &sm.kv_full[vs], 0, row, 2 * it.h, pol_kv);
+            last_load = (int)nv_load;
           }
         }
         ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
         if (ok && j == it.nk - 1 && it.last_rows < kBN) {
           // zero the rows past the sequence's keys before the MMA reads this V tile
-          ok = __all_sync(kFull, wait_parity(&sm.v_full[st], (g / kStages) & 1, p.err));
+          ok = __all_sync(kFull, wait_parity(&sm.kv_full[vs], (nv_load / kSlots) & 1, p.err));
           if (ok) {
-            uint8_t *vt = sm.v[st];
+            uint8_t *vt = sm.kv[vs];
             for (int idx = lane; idx < (kBN - it.last_rows) * 16; idx += 32) {
               const int r = it.last_rows + (idx >> 4), c = idx & 15;
               *reinterpret_cast<uint4 *>(vt + (c >> 3) * kHalfBytes + r * 128 + (c & 7) * 16) =
@@ -362,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             fence_async_shared();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.v_fixed[st]);
+            if (lane == 0) mbar_arrive(&sm.v_fixed[vs]);
           }
         }
       }
@@ -371,10 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool drained = true;
       for (int a = 0; a < 2 && q_loads > 0; ++a)
         drained = drained && wait_parity(&sm.q_full[a], (q_loads - 1) & 1, p.err);
-      for (int t = max(0, last_k - kStages + 1); drained && t <= last_k; ++t)
-        drained = wait_parity(&sm.k_full[t % kStages], (t / kStages) & 1, p.err);
-      for (int t = max(0, last_v - kStages + 1); drained && t <= last_v; ++t)
-        drained = wait_parity(&sm.v_full[t % kStages], (t / kStages) & 1, p.err);
+      for (int t = max(0, last_load - kSlots + 1); drained && t <= last_load; ++t)
+        drained = wait_parity(&sm.kv_full[t % kSlots], (t / kSlots) & 1, p.err);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ UMMA issuer
@@ -382,10 +379,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdS = idesc_bf16_f32(kBM, kBN, 0, 0);  // Q (K-major) x K (K-major)
       constexpr uint32_t kIdO = idesc_bf16_f32(kBM, kD, 0, 1);   // P (TMEM) x V (MN-major)
       const uint32_t qa0 = smem_addr(sm.q[0]), qa1 = smem_addr(sm.q[1]);
-      const uint32_t ka0 = smem_addr(sm.k[0]), ka1 = smem_addr(sm.k[1]);
-      const uint32_t va0 = smem_addr(sm.v[0]), va1 = smem_addr(sm.v[1]);
-      uint32_t taken = 0, q_loads = 0, g = 0, fix0 = 0, fix1 = 0;
+      const uint32_t kv0 = smem_addr(sm.kv[0]);
+      uint32_t taken = 0, q_loads = 0, g = 0;
+      uint32_t fix_parity = 0;  // bit s: parity of the next v_fixed phase of slot s
       bool ok = true;
+      // V(j) of tile gg: wait for the load (or, for a fixed last tile, for the fix)
+      auto v_ready = [&](uint32_t gg, bool fixed) -> bool {
+        const uint32_t n = 2 * gg + 1, vs = n % kSlots;
+        if (fixed) {
+          const bool r = wait_parity(&sm.v_fixed[vs], (fix_parity >> vs) & 1, p.err);
+          fix_parity ^= 1u << vs;
+          return r;
+        }
+        return wait_parity(&sm.kv_full[vs], (n / kSlots) & 1, p.err);
+      };
       while (ok) {
         const Item it = take_item(sm, taken, p.err);
         mbar_arrive(&sm.item_empty[taken % kRing]);
@@ -395,9 +402,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nk = it.nk;
         const bool fix_v = it.last_rows < kBN;
         for (int j = 0; j < nk; ++j, ++g) {
-          const uint32_t st = g & 1;
-          const uint32_t ka = st ? ka1 : ka0;
-          ok = wait_parity(&sm.k_full[st], (g >> 1) & 1, p.err);
+          const uint32_t ks = (2 * g) % kSlots;
+          const uint32_t ka = kv0 + ks * kTileBytes;
+          ok = wait_parity(&sm.kv_full[ks], ((2 * g) / kSlots) & 1, p.err);
           if (!ok) break;
           tc_fence_after_sync();
           // S_0(j)
@@ -411,14 +418,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j == nk - 1) umma_commit(&sm.q_empty[0]);
           // O_1 += P_1(j-1) V(j-1)  (never the last tile here)
           if (j > 0) {
-            const uint32_t gp = g - 1, sp = gp & 1;
-            ok = wait_parity(&sm.p_full[1], gp & 1, p.err) &&
-                 wait_parity(&sm.v_full[sp], (gp >> 1) & 1, p.err);
+            const uint32_t gp = g - 1, vs = (2 * gp + 1) % kSlots;
+            ok = wait_parity(&sm.p_full[1], gp & 1, p.err) && v_ready(gp, false);
             if (!ok) break;
             tc_fence_after_sync();
-            mma_pv(tmem + 384, tmem + 128, sp ? va1 : va0, kIdO, j - 1 > 0);
+            mma_pv(tmem + 384, tmem + 128, kv0 + vs * kTileBytes, kIdO, j - 1 > 0);
             umma_commit(&sm.o_full[1]);
-            umma_commit(&sm.v_empty[sp]);
+            umma_commit(&sm.kv_empty[vs]);
           }
           // S_1(j)
           if (j == 0) {
@@ -429,32 +435,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_qk(tmem + 128, qa1, ka, kIdS);
           umma_commit(&sm.s_full[1]);
           if (j == nk - 1) umma_commit(&sm.q_empty[1]);
-          umma_commit(&sm.k_empty[st]);
-          // O_0 += P_0(j) V(j)
-          ok = wait_parity(&sm.p_full[0], g & 1, p.err) &&
-               ((j == nk - 1 && fix_v)
-                    ? wait_parity(&sm.v_fixed[st], (st ? fix1 : fix0) & 1, p.err)
-                    : wait_parity(&sm.v_full[st], (g >> 1) & 1, p.err));
+          umma_commit(&sm.kv_empty[ks]);
+          // O_0 += P_0(j) V(j); for a fixed last tile this wait also covers O_1's use below
+          ok = wait_parity(&sm.p_full[0], g & 1, p.err) && v_ready(g, j == nk - 1 && fix_v);
           if (!ok) break;
           tc_fence_after_sync();
-          mma_pv(tmem + 256, tmem, st ? va1 : va0, kIdO, j > 0);
+          mma_pv(tmem + 256, tmem, kv0 + ((2 * g + 1) % kSlots) * kTileBytes, kIdO, j > 0);
           umma_commit(&sm.o_full[0]);
         }
         if (!ok) break;
-        {  // O_1 += P_1(last) V(last)
-          const uint32_t gp = g - 1, sp = gp & 1;
-          ok = wait_parity(&sm.p_full[1], gp & 1, p.err) &&
-               (fix_v ? wait_parity(&sm.v_fixed[sp], (sp ? fix1 : fix0) & 1, p.err)
-                      : wait_parity(&sm.v_full[sp], (gp >> 1) & 1, p.err));
+        {  // O_1 += P_1(last) V(last): V(last) is ready (waited above)
+          const uint32_t gp = g - 1, vs = (2 * gp + 1) % kSlots;
+          ok = wait_parity(&sm.p_full[1], gp & 1, p.err);
           if (!ok) break;
           tc_fence_after_sync();
-          mma_pv(tmem + 384, tmem + 128, sp ? va1 : va0, kIdO, nk > 1);
+          mma_pv(tmem + 384, tmem + 128, kv0 + vs * kTileBytes, kIdO, nk > 1);
           umma_commit(&sm.o_full[1]);
-          umma_commit(&sm.v_empty[sp]);
-          if (fix_v) {
-            if (sp) ++fix1;
-            else ++fix0;
-          }
+          umma_commit(&sm.kv_empty[vs]);
         }
         ++q_loads;
       }
