@@ -200,7 +200,9 @@ class DecodeStep:
                 events[-1].record()
 
     def launches_per_step(self):
-        return self.layers * (2 + (1 if self.splits_workspace > 0 else 0))
+        # kv_store + split kernel, + the combine kernel when the context is split (the
+        # workspace then holds partial outputs beyond its 16-byte work counter)
+        return self.layers * (2 + (1 if self.splits_workspace > 16 else 0))
 
 
 def time_e2e(step: DecodeStep, steps: int):
@@ -248,6 +250,38 @@ def time_prefill_store(pkv, iters: int = 20):
     del k, v, kc, vc
     return {"tokens": T, "gbs": nbytes / t / 1e9, "us": t * 1e6,
             "bytes": nbytes, "l2": "inputs (1.18 GB) larger than L2"}
+
+
+def time_decode_shape(pkv, batch: int, ctx: int, hbm_peak: float, iters: int = 20):
+    """Paged decode attention alone on `batch` sequences of `ctx` tokens (blocks drawn at
+    random). Small batches rotate over enough disjoint copies of the pool region that the
+    timed reads (>= 1 GB across the rotation) do not come from L2."""
+    per = batch * (-(-ctx // BS))
+    reps = max(1, -(-(1 << 30) // (per * BS * ROW_BYTES * 2)))
+    lay = w.decode_layout(np.full(batch * reps, ctx, np.int32), per * reps + 8, w.rng(5 + batch))
+    kc = w.device_bf16_normal((lay.num_blocks, BS, HKV, D), 601)
+    vc = w.device_bf16_normal((lay.num_blocks, BS, HKV, D), 602)
+    q = w.device_bf16_normal((batch, HQ, D), 603)
+    out = torch.empty_like(q)
+    tables = [torch.from_numpy(lay.block_tables[r * batch:(r + 1) * batch].copy()).cuda()
+              for r in range(reps)]
+    cl = torch.full((batch,), ctx, dtype=torch.int32, device="cuda")
+    ws = pkv.decode_workspace(batch, HQ, HKV, D, ctx, 0)
+    for r in range(min(reps, 3)):
+        pkv.paged_decode_attn(q, kc, vc, tables[r], cl, ctx, D ** -0.5, workspace=ws, out=out)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for i in range(iters):
+        pkv.paged_decode_attn(q, kc, vc, tables[i % reps], cl, ctx, D ** -0.5, workspace=ws,
+                              out=out)
+    e1.record()
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / 1e3 / iters
+    nbytes = decode_bytes(np.full(batch, ctx), tables[0].shape[1])["decode"]
+    del kc, vc
+    return {"batch": batch, "ctx": ctx, "us": t * 1e6, "gbs": nbytes / t / 1e9,
+            "frac_of_hbm_peak": nbytes / t / 1e9 / hbm_peak, "kv_tokens_per_s": batch * ctx / t}
 
 
 def time_prefill(pkv, iters: int = 10):
@@ -368,6 +402,11 @@ def run_ours(args):
 
     extra = {}
     if not args.skip_extra:
+        extra["decode_long_context"] = time_decode_shape(pkv, 32, 32768, hbm_peak)
+        extra["decode_batch_sweep"] = [
+            {k: v for k, v in time_decode_shape(pkv, b, 1024, hbm_peak).items()
+             if k in ("batch", "us", "gbs", "frac_of_hbm_peak")}
+            for b in (1, 2, 4, 8, 16, 32, 64, 128, 256, 512)]
         extra["kv_store_prefill"] = time_prefill_store(pkv)
         extra["prefill"] = time_prefill(pkv)
         if "tflops" in extra["prefill"]:

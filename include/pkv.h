@@ -102,11 +102,12 @@ pkv_status pkv_kv_store(const void *k, int64_t k_tok_stride, const void *v, int6
                         int32_t head_dim, void *stream);
 
 /*
- * Bytes of device workspace that pkv_paged_decode_attn needs for these sizes (0 when the
- * chosen split count is 1). `num_splits` must be the value later passed to the call (0 =
- * automatic choice, made from the sizes and the current device's SM count). The workspace
- * holds each split's partial output [batch, num_q_heads, splits, head_dim] fp32 and its
- * log-sum-exp [batch, num_q_heads, splits] fp32. Returns 0 for invalid sizes.
+ * Bytes of device workspace that pkv_paged_decode_attn needs for these sizes (at least 16).
+ * `num_splits` must be the value later passed to the call (0 = automatic choice, made from
+ * the sizes and the current device's SM count). The workspace holds each split's partial
+ * output [batch, num_q_heads, splits, head_dim] fp32 and its log-sum-exp [batch,
+ * num_q_heads, splits] fp32 (when there is more than one split), then the persistent
+ * kernel's work counter, which the call resets on its stream. Returns 0 for invalid sizes.
  */
 size_t pkv_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                   int32_t head_dim, int32_t max_context_len,
@@ -136,8 +137,9 @@ size_t pkv_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t nu
  *                shorter sequences use fewer splits). Results are identical for any
  *                physical placement of the blocks; they differ by rounding across values of
  *                num_splits.
- * workspace:     pkv_decode_workspace_bytes(...) bytes, 16-byte aligned (may be NULL when
- *                that is 0). Contents on entry are ignored.
+ * workspace:     pkv_decode_workspace_bytes(...) bytes, 16-byte aligned, private to this
+ *                call while it runs (calls that may overlap need separate workspaces).
+ *                Contents on entry are ignored.
  * out:           [batch, num_q_heads, head_dim] bf16.
  * Implemented: head_dim == 128, block_size a multiple of 256 (the pages: block size must be
  * a multiple of 256), any num_q_heads / num_kv_heads, q, pools and out 16-byte aligned.

@@ -4,25 +4,28 @@
 // one query token per sequence attends over its context, whose K/V rows are gathered
 // through the sequence's block table. GQA: query head hq reads KV head hq / G.
 //
-// Work unit (one CTA): sequence b, KV head h, up to two of the G query heads of h (so a
-// CTA reads each K/V byte once for both heads of a Qwen3 group), and one split: the
-// logical tokens [s * chunk, min((s + 1) * chunk, ctx_b)). chunk is a multiple of the 64-
-// token tile (up to 1024 tokens when there is enough parallelism) and the block size is a
-// multiple of 256, so a tile never straddles a block.
+// Work unit: sequence b, KV head h, up to two of the G query heads of h (so each K/V byte is
+// read once for both heads of a Qwen3 group), and one split: the logical tokens
+// [s * chunk, min((s + 1) * chunk, ctx_b)). chunk is a multiple of the 64-token tile and the
+// block size a multiple of 256, so a tile never straddles a block.
 //
-// Pipeline (per CTA, 8 consumer warps + 1 producer warp):
-//   producer  -- one thread looks up block_tables[b][pos / block_size] and issues two TMA
-//                tensor loads per tile (K and V: 64 tokens x 256 bytes of head h each,
-//                128-byte swizzled) into a 3-stage ring guarded by full/empty mbarriers;
-//   consumers -- warp w owns tokens [8w, 8w + 8) of every tile and keeps its own online-
-//                softmax state (running max m, sum l, accumulator acc) in registers:
+// Persistent kernel: two CTAs per SM take units from a global queue (one atomic counter in
+// the workspace; units ordered split-major with the KV heads of a sequence adjacent, so the
+// CTAs reading one sequence's rows run together). Per CTA, 8 consumer warps + 1 producer
+// warp:
+//   producer  -- takes a unit, hands it to the consumers through a 4-slot ring (the unit's
+//                q rows arrive by a 1-D bulk copy into the ring slot), then streams the
+//                unit's tiles: per 64-token tile it looks up block_tables[b][pos / bs] and
+//                issues two TMA tensor loads (K and V, 64 tokens x 256 bytes of head h,
+//                128-byte swizzled) into a 3-stage ring, without stopping between units;
+//   consumers -- warp w owns tokens [8w, 8w + 8) of every tile with its own online softmax:
 //                  QK:  4 lanes per token, 32 dims per lane, mixed-precision bf16 FMAs on
 //                       packed q (no conversions), reduced with 2 shuffles;
 //                  PV:  16 lanes per token (8 dims each), two tokens per instruction,
 //                       packed fp32x2 FMAs;
-//                at the end the 8 warp states are merged through shared memory.
-// With one split the CTA writes bf16 output directly; otherwise it writes its normalised
-// partial output and log2-sum-exp, and decode_combine_kernel merges the splits.
+//                at the end of a unit the 8 warp states are merged through shared memory.
+// With one split a unit writes bf16 output; otherwise it writes its normalised partial
+// output and log2-sum-exp, and decode_combine_kernel merges the splits.
 //
 // Algorithmic HBM bytes per (sequence, KV head, token): 256 (K) + 256 (V).
 #include <math.h>
@@ -39,10 +42,15 @@ constexpr int kD = 128;
 constexpr int kTile = 64;
 constexpr int kConsumerWarps = 8;
 constexpr int kStages = 3;
+constexpr int kRing = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kTileBytes = kTile * kD * 2;  // one head's K (or V) for 64 tokens: 16 KiB
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned kFull = 0xffffffffu;
+
+struct Unit {
+  int32_t b, s, xg, ntiles;  // ntiles < 0: no more work
+};
 
 template <int GC>
 struct DecodeSmem {
@@ -51,8 +59,12 @@ struct DecodeSmem {
   float acc[kConsumerWarps][GC][kD];
   float m[kConsumerWarps][GC];
   float l[kConsumerWarps][GC];
+  uint16_t qs[kRing][GC][kD];  // q rows of the queued units
+  Unit unit[kRing];
   uint64_t full[kStages];
   uint64_t empty[kStages];
+  uint64_t unit_full[kRing];
+  uint64_t unit_empty[kRing];
 };
 
 // Byte offset of 16-byte chunk j (dims 8j..8j+7) of token t inside a swizzled tile. The TMA
@@ -63,46 +75,39 @@ __device__ __forceinline__ uint32_t tile_offset(int t, int j) {
   return (uint32_t)((r << 7) | (((j & 7) ^ (r & 7)) << 4));
 }
 
+struct DecodeParams {
+  const uint16_t *q;
+  const int32_t *block_tables;
+  const int32_t *context_lens;
+  float *part_o;
+  float *part_lse;
+  uint16_t *out;
+  int32_t *queue;
+  unsigned int *err;
+  int64_t num_blocks;
+  int64_t cap;  // longest context the table rows and the split grid can address
+  int32_t table_width;
+  int32_t batch;
+  int32_t num_q_heads;
+  int32_t group;
+  int32_t head_groups;
+  int32_t xgroups;  // num_kv_heads * head_groups
+  int32_t block_size;
+  int32_t chunk;
+  int32_t splits;
+  int32_t units;    // splits * batch * xgroups
+  float qscale;
+};
+
 template <int GC>
 // 96 registers: warps are placed on the 4 SM sub-partitions (16K registers each), so two
 // 9-warp CTAs (5 warps on some sub-partitions) fit only at <= 102 registers per thread.
 __global__ void __maxnreg__(96)
     decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
-                        const __grid_constant__ CUtensorMap vmap, const uint16_t *__restrict__ q,
-                        const int32_t *__restrict__ block_tables, int32_t table_width,
-                        const int32_t *__restrict__ context_lens, int32_t num_q_heads,
-                        int32_t group, int32_t head_groups, int32_t block_size,
-                        int64_t num_blocks, int32_t chunk, int32_t splits, float qscale,
-                        float *__restrict__ part_o, float *__restrict__ part_lse,
-                        uint16_t *__restrict__ out, unsigned int *err) {
-  const int xg = blockIdx.x;
-  const int h = xg / head_groups;
-  const int hq0 = h * group + (xg % head_groups) * GC;
-  const int s = blockIdx.y;
-  const int b = blockIdx.z;
-
-  // context length, clamped to what the table row and the split grid can address
-  const int64_t cap64 = min((int64_t)table_width * block_size, (int64_t)splits * chunk);
-  int64_t L = context_lens[b];
-  if (L < 0 || L > cap64) {
-    if (s == 0 && xg == 0 && threadIdx.x == 0) record_error(err, 4u /* CONTEXT_RANGE */);
-    L = L < 0 ? 0 : cap64;
-  }
-  const int tok_begin = s * chunk;
-  if (tok_begin >= L) {
-    if (L == 0 && splits == 1 && threadIdx.x < GC * kD) {  // empty context: zeros
-      const int g = threadIdx.x / kD, d = threadIdx.x % kD;
-      out[((int64_t)b * num_q_heads + hq0 + g) * kD + d] = 0;
-    }
-    return;
-  }
-  const int tok_end = (int)min(L, (int64_t)tok_begin + chunk);
-  const int ntiles = (tok_end - tok_begin + kTile - 1) / kTile;
-
+                        const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
   DecodeSmem<GC> &sm = *reinterpret_cast<DecodeSmem<GC> *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -110,9 +115,13 @@ __global__ void __maxnreg__(96)
       mbar_init(&sm.full[i], 1);
       mbar_init(&sm.empty[i], kConsumerWarps);
     }
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(&sm.unit_full[i], 1);
+      mbar_init(&sm.unit_empty[i], kConsumerWarps);
+    }
     fence_mbar_init();
   }
-  if (__syncthreads_or(threadIdx.x == 0 && aborted(err))) return;  // uniform across the CTA
+  if (__syncthreads_or(threadIdx.x == 0 && aborted(p.err))) return;  // uniform across the CTA
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------------ producer
@@ -120,34 +129,78 @@ __global__ void __maxnreg__(96)
     prefetch_tensormap(&kmap);
     prefetch_tensormap(&vmap);
     const uint64_t policy = policy_evict_first();
-    const int32_t *table = block_tables + (int64_t)b * table_width;
-    int issued = 0;
-    for (int it = 0; it < ntiles; ++it) {
-      const int stage = it % kStages;
-      if (it >= kStages && !wait_parity(&sm.empty[stage], ((it / kStages) - 1) & 1, err)) {
-        record_error(err, 16u /* TIMEOUT */);
+    uint32_t pushed = 0, tiles = 0;
+    bool ok = true;
+    while (ok) {
+      // next unit with work (or one that must write zeros); ntiles < 0 ends the walk
+      Unit un{0, 0, 0, -1};
+      while (true) {
+        const int u = atomicAdd(p.queue, 1);
+        if (u >= p.units) break;
+        const int s = u / (p.batch * p.xgroups);
+        const int r = u % (p.batch * p.xgroups);
+        const int b = r / p.xgroups, xg = r % p.xgroups;
+        int64_t L = p.context_lens[b];
+        if (L < 0 || L > p.cap) {
+          if (s == 0 && xg == 0) record_error(p.err, 4u /* CONTEXT_RANGE */);
+          L = L < 0 ? 0 : p.cap;
+        }
+        const int64_t begin = (int64_t)s * p.chunk;
+        if (begin < L) {
+          const int64_t end = min(L, begin + p.chunk);
+          un = Unit{b, s, xg, (int)((end - begin + kTile - 1) / kTile)};
+          break;
+        }
+        if (L == 0 && s == 0 && p.splits == 1) {  // empty context, direct output: zeros
+          un = Unit{b, s, xg, 0};
+          break;
+        }
+      }
+      const int slot = pushed % kRing;
+      if (pushed >= kRing &&
+          !wait_parity(&sm.unit_empty[slot], ((pushed / kRing) - 1) & 1, p.err)) {
+        ok = false;
         break;
       }
-      const int pos = tok_begin + it * kTile;
-      const int64_t blk = table[pos / block_size];
-      int32_t row;
-      if (blk < 0 || blk >= num_blocks) {
-        record_error(err, 2u /* BLOCK_RANGE */);
-        row = -2 * kTile;  // wholly outside the pool: TMA fills zeros, nothing is read
-      } else {
-        row = (int32_t)(blk * block_size + pos % block_size);
+      sm.unit[slot] = un;
+      ++pushed;
+      if (un.ntiles < 0) {
+        mbar_arrive(&sm.unit_full[slot]);
+        break;
       }
-      mbar_arrive_expect_tx(&sm.full[stage], 2 * kTileBytes);
-      tma_load_3d(sm.k[stage], &kmap, &sm.full[stage], 0, 2 * h, row, policy);
-      tma_load_3d(sm.v[stage], &vmap, &sm.full[stage], 0, 2 * h, row, policy);
-      ++issued;
+      const int h = un.xg / p.head_groups;
+      const int hq0 = h * p.group + (un.xg % p.head_groups) * GC;
+      mbar_arrive_expect_tx(&sm.unit_full[slot], GC * kD * 2);
+      bulk_copy_g2s(sm.qs[slot], p.q + ((int64_t)un.b * p.num_q_heads + hq0) * kD, GC * kD * 2,
+                    &sm.unit_full[slot]);
+      const int32_t *table = p.block_tables + (int64_t)un.b * p.table_width;
+      const int tok_begin = un.s * p.chunk;
+      for (int it = 0; it < un.ntiles; ++it, ++tiles) {
+        const int stage = tiles % kStages;
+        if (tiles >= kStages && !wait_parity(&sm.empty[stage], ((tiles / kStages) - 1) & 1, p.err)) {
+          ok = false;
+          break;
+        }
+        const int pos = tok_begin + it * kTile;
+        const int64_t blk = table[pos / p.block_size];
+        int32_t row;
+        if (blk < 0 || blk >= p.num_blocks) {
+          record_error(p.err, 2u /* BLOCK_RANGE */);
+          row = -2 * kTile;  // wholly outside the pool: TMA fills zeros, nothing is read
+        } else {
+          row = (int32_t)(blk * p.block_size + pos % p.block_size);
+        }
+        mbar_arrive_expect_tx(&sm.full[stage], 2 * kTileBytes);
+        tma_load_3d(sm.k[stage], &kmap, &sm.full[stage], 0, 2 * h, row, policy);
+        tma_load_3d(sm.v[stage], &vmap, &sm.full[stage], 0, 2 * h, row, policy);
+      }
     }
     // keep the CTA alive until every copy it issued has landed
-    for (int it = max(0, issued - kStages); it < issued; ++it)
-      if (!wait_parity(&sm.full[it % kStages], (it / kStages) & 1, err)) {
-        record_error(err, 16u);
-        break;
-      }
+    bool drained = true;
+    for (uint32_t t = tiles > kStages ? tiles - kStages : 0; drained && t < tiles; ++t)
+      drained = wait_parity(&sm.full[t % kStages], (t / kStages) & 1, p.err);
+    for (uint32_t k = pushed > kRing ? pushed - kRing : 0; drained && k < pushed; ++k)
+      drained = wait_parity(&sm.unit_full[k % kRing], (k / kRing) & 1, p.err);
     return;
   }
 
@@ -162,184 +215,205 @@ __global__ void __maxnreg__(96)
   const int dl = lane & 15;   // PV: chunk (dims 8dl..8dl+7)
   const int t_qk = warp * 8 + tq;
   const int chunk0 = 8 * (sub & 1) + 4 * (sub >> 1);  // chunks chunk0 + r, r = 0..3
-  // shared-memory offsets inside a tile are the same for every tile
   uint32_t off_qk[4], off_pv[4];
 #pragma unroll
   for (int r = 0; r < 4; ++r) off_qk[r] = tile_offset(t_qk, chunk0 + r);
 #pragma unroll
   for (int i = 0; i < 4; ++i) off_pv[i] = tile_offset(warp * 8 + 2 * i + hw, dl);
 
-  // q stays packed bf16: QK uses mixed-precision FMAs, the scale is applied to the score
-  uint32_t qw[GC][4][4];
+  // Every decision to leave the unit loop is taken by all 8 consumer warps together (a
+  // barrier reduction), so no warp can be left waiting in a merge barrier.
+  uint32_t taken = 0, tiles = 0;
+  while (true) {
+    const int slot = taken % kRing;
+    const bool got = wait_parity(&sm.unit_full[slot], (taken / kRing) & 1, p.err);
+    if (barrier_or(3, kConsumerWarps * 32, !got)) break;
+    const Unit un = sm.unit[slot];
+    ++taken;
+    if (un.ntiles < 0) break;
+    const int h = un.xg / p.head_groups;
+    const int hq0 = h * p.group + (un.xg % p.head_groups) * GC;
+    // q stays packed bf16: QK uses mixed-precision FMAs, the scale is applied to the score
+    uint32_t qw[GC][4][4];
 #pragma unroll
-  for (int g = 0; g < GC; ++g) {
-    const uint4 *qrow = reinterpret_cast<const uint4 *>(q + ((int64_t)b * num_q_heads + hq0 + g) * kD);
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const uint4 w4 = __ldg(qrow + chunk0 + r);
-      qw[g][r][0] = w4.x;
-      qw[g][r][1] = w4.y;
-      qw[g][r][2] = w4.z;
-      qw[g][r][3] = w4.w;
-    }
-  }
-
-  float m_run[GC], l_run[GC];
-  float2 acc[GC][4];  // dims 8dl + 2e, 8dl + 2e + 1
-#pragma unroll
-  for (int g = 0; g < GC; ++g) {
-    m_run[g] = -INFINITY;
-    l_run[g] = 0.f;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) acc[g][e] = make_float2(0.f, 0.f);
-  }
-
-  for (int it = 0; it < ntiles; ++it) {
-    const int stage = it % kStages;
-    // warp-uniform: the loop body uses full-warp shuffles
-    if (!__all_sync(kFull, wait_parity(&sm.full[stage], (it / kStages) & 1, err))) break;
-    const uint8_t *kt = sm.k[stage];
-    const uint8_t *vt = sm.v[stage];
-    const int n_valid = tok_end - (tok_begin + it * kTile);  // >= 1; < 64 only in a last tile
-
-    // ---- scores for token t_qk (log2 domain)
-    float sc[GC];
-    {
-      float s_lo[GC], s_hi[GC];
-#pragma unroll
-      for (int g = 0; g < GC; ++g) s_lo[g] = s_hi[g] = 0.f;
+    for (int g = 0; g < GC; ++g)
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const uint4 k4 = *reinterpret_cast<const uint4 *>(kt + off_qk[r]);
-        const uint32_t w[4] = {k4.x, k4.y, k4.z, k4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-#pragma unroll
-          for (int g = 0; g < GC; ++g) fma_bf16_pairs(qw[g][r][e], w[e], s_lo[g], s_hi[g]);
+        const uint4 w4 = *reinterpret_cast<const uint4 *>(&sm.qs[slot][g][8 * (chunk0 + r)]);
+        qw[g][r][0] = w4.x;
+        qw[g][r][1] = w4.y;
+        qw[g][r][2] = w4.z;
+        qw[g][r][3] = w4.w;
       }
-#pragma unroll
-      for (int g = 0; g < GC; ++g) {
-        float v = s_lo[g] + s_hi[g];
-        v += __shfl_xor_sync(kFull, v, 4);   // the 4 lanes of a token differ in lane bits 2-3
-        v += __shfl_xor_sync(kFull, v, 8);
-        sc[g] = v * qscale;
-      }
-    }
-    if (n_valid < kTile) {
-#pragma unroll
-      for (int g = 0; g < GC; ++g)
-        if (t_qk >= n_valid) sc[g] = -INFINITY;
-    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.unit_empty[slot]);
 
-    // ---- online softmax over the warp's 8 tokens
-    float p[GC];
-    bool any = false;
+    int64_t L = p.context_lens[un.b];
+    L = L < 0 ? 0 : (L > p.cap ? p.cap : L);
+    const int tok_begin = un.s * p.chunk;
+    const int tok_end = (int)min(L, (int64_t)tok_begin + p.chunk);
+
+    float m_run[GC], l_run[GC];
+    float2 acc[GC][4];  // dims 8dl + 2e, 8dl + 2e + 1
 #pragma unroll
     for (int g = 0; g < GC; ++g) {
-      float mx = sc[g];  // the warp's 8 tokens differ in lane bits 0, 1 and 4
-      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
-      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
-      if (mx > m_run[g]) {  // warp-uniform: every lane holds the same maxima
-        const float alpha = fast_exp2(m_run[g] - mx);
-        l_run[g] *= alpha;
+      m_run[g] = -INFINITY;
+      l_run[g] = 0.f;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          acc[g][e].x *= alpha;
-          acc[g][e].y *= alpha;
-        }
-        m_run[g] = mx;
-      }
-      if (m_run[g] != -INFINITY) {
-        any = true;
-        p[g] = fast_exp2(sc[g] - m_run[g]);
-        float ps = p[g];
-        ps += __shfl_xor_sync(kFull, ps, 1);
-        ps += __shfl_xor_sync(kFull, ps, 2);
-        ps += __shfl_xor_sync(kFull, ps, 16);
-        l_run[g] += ps;
-      } else {
-        p[g] = 0.f;
-      }
+      for (int e = 0; e < 4; ++e) acc[g][e] = make_float2(0.f, 0.f);
     }
 
-    // ---- acc += p v, two tokens per instruction (half-warp hw takes token 2i + hw)
-    if (any) {
+    bool ok = true;
+    for (int it = 0; it < un.ntiles; ++it, ++tiles) {
+      const int stage = tiles % kStages;
+      // warp-uniform: the loop body uses full-warp shuffles
+      if (!__all_sync(kFull, wait_parity(&sm.full[stage], (tiles / kStages) & 1, p.err))) {
+        ok = false;
+        break;
+      }
+      const uint8_t *kt = sm.k[stage];
+      const uint8_t *vt = sm.v[stage];
+      const int n_valid = tok_end - (tok_begin + it * kTile);  // >= 1; < 64 only in a last tile
+
+      // ---- scores for token t_qk (log2 domain)
+      float sc[GC];
+      {
+        float s_lo[GC], s_hi[GC];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int tt = 2 * i + hw;
-        float2 pv[GC];
+        for (int g = 0; g < GC; ++g) s_lo[g] = s_hi[g] = 0.f;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const uint4 k4 = *reinterpret_cast<const uint4 *>(kt + off_qk[r]);
+          const uint32_t w[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+#pragma unroll
+            for (int g = 0; g < GC; ++g) fma_bf16_pairs(qw[g][r][e], w[e], s_lo[g], s_hi[g]);
+        }
 #pragma unroll
         for (int g = 0; g < GC; ++g) {
-          const float x = __shfl_sync(kFull, p[g], (tt & 3) | ((tt >> 2) << 4));
-          pv[g] = make_float2(x, x);
+          float v = s_lo[g] + s_hi[g];
+          v += __shfl_xor_sync(kFull, v, 4);   // the 4 lanes of a token differ in lane bits 2-3
+          v += __shfl_xor_sync(kFull, v, 8);
+          sc[g] = v * p.qscale;
         }
-        if (n_valid >= kTile || warp * 8 + tt < n_valid) {
-          const uint4 v4 = *reinterpret_cast<const uint4 *>(vt + off_pv[i]);
-          const uint32_t w[4] = {v4.x, v4.y, v4.z, v4.w};
+      }
+      if (n_valid < kTile) {
+#pragma unroll
+        for (int g = 0; g < GC; ++g)
+          if (t_qk >= n_valid) sc[g] = -INFINITY;
+      }
+
+      // ---- online softmax over the warp's 8 tokens
+      float pr[GC];
+      bool any = false;
+#pragma unroll
+      for (int g = 0; g < GC; ++g) {
+        float mx = sc[g];  // the warp's 8 tokens differ in lane bits 0, 1 and 4
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+        if (mx > m_run[g]) {  // warp-uniform: every lane holds the same maxima
+          const float alpha = fast_exp2(m_run[g] - mx);
+          l_run[g] *= alpha;
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float2 vf = make_float2(bf16_lo(w[e]), bf16_hi(w[e]));
+            acc[g][e].x *= alpha;
+            acc[g][e].y *= alpha;
+          }
+          m_run[g] = mx;
+        }
+        if (m_run[g] != -INFINITY) {
+          any = true;
+          pr[g] = fast_exp2(sc[g] - m_run[g]);
+          float ps = pr[g];
+          ps += __shfl_xor_sync(kFull, ps, 1);
+          ps += __shfl_xor_sync(kFull, ps, 2);
+          ps += __shfl_xor_sync(kFull, ps, 16);
+          l_run[g] += ps;
+        } else {
+          pr[g] = 0.f;
+        }
+      }
+
+      // ---- acc += p v, two tokens per instruction (half-warp hw takes token 2i + hw)
+      if (any) {
 #pragma unroll
-            for (int g = 0; g < GC; ++g) acc[g][e] = ffma2(pv[g], vf, acc[g][e]);
+        for (int i = 0; i < 4; ++i) {
+          const int tt = 2 * i + hw;
+          float2 pv[GC];
+#pragma unroll
+          for (int g = 0; g < GC; ++g) {
+            const float x = __shfl_sync(kFull, pr[g], (tt & 3) | ((tt >> 2) << 4));
+            pv[g] = make_float2(x, x);
+          }
+          if (n_valid >= kTile || warp * 8 + tt < n_valid) {
+            const uint4 v4 = *reinterpret_cast<const uint4 *>(vt + off_pv[i]);
+            const uint32_t w[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 vf = make_float2(bf16_lo(w[e]), bf16_hi(w[e]));
+#pragma unroll
+              for (int g = 0; g < GC; ++g) acc[g][e] = ffma2(pv[g], vf, acc[g][e]);
+            }
           }
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.empty[stage]);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.empty[stage]);
-  }
 
-  // ---- merge: half-warps, then the 8 warps through shared memory
+    // ---- merge: half-warps, then the 8 warps through shared memory
 #pragma unroll
-  for (int g = 0; g < GC; ++g)
+    for (int g = 0; g < GC; ++g)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      acc[g][e].x += __shfl_xor_sync(kFull, acc[g][e].x, 16);
-      acc[g][e].y += __shfl_xor_sync(kFull, acc[g][e].y, 16);
-    }
-  if (lane < 16) {
-#pragma unroll
-    for (int g = 0; g < GC; ++g) {
-      float4 *dst = reinterpret_cast<float4 *>(&sm.acc[warp][g][8 * dl]);
-      dst[0] = make_float4(acc[g][0].x, acc[g][0].y, acc[g][1].x, acc[g][1].y);
-      dst[1] = make_float4(acc[g][2].x, acc[g][2].y, acc[g][3].x, acc[g][3].y);
-    }
-  }
-  if (lane == 0) {
-#pragma unroll
-    for (int g = 0; g < GC; ++g) {
-      sm.m[warp][g] = m_run[g];
-      sm.l[warp][g] = l_run[g];
-    }
-  }
-  named_barrier_sync(1, kConsumerWarps * 32);
-
-  const int g = threadIdx.x / kD;
-  const int d = threadIdx.x % kD;
-  if (g < GC) {
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm.m[w][g]);
-    float o = 0.f, lse = -INFINITY;
-    if (M != -INFINITY) {
-      float lsum = 0.f, osum = 0.f;
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        const float f = fast_exp2(sm.m[w][g] - M);
-        lsum = fmaf(sm.l[w][g], f, lsum);
-        osum = fmaf(sm.acc[w][g][d], f, osum);
+      for (int e = 0; e < 4; ++e) {
+        acc[g][e].x += __shfl_xor_sync(kFull, acc[g][e].x, 16);
+        acc[g][e].y += __shfl_xor_sync(kFull, acc[g][e].y, 16);
       }
-      o = osum / lsum;
-      lse = M + log2f(lsum);
+    if (lane < 16) {
+#pragma unroll
+      for (int g = 0; g < GC; ++g) {
+        float4 *dst = reinterpret_cast<float4 *>(&sm.acc[warp][g][8 * dl]);
+        dst[0] = make_float4(acc[g][0].x, acc[g][0].y, acc[g][1].x, acc[g][1].y);
+        dst[1] = make_float4(acc[g][2].x, acc[g][2].y, acc[g][3].x, acc[g][3].y);
+      }
     }
-    const int64_t row = (int64_t)b * num_q_heads + hq0 + g;
-    if (splits == 1) {
-      out[row * kD + d] = bf16_bits_rn(o);
-    } else {
-      part_o[(row * splits + s) * kD + d] = o;
-      if (d == 0) part_lse[row * splits + s] = lse;
+    if (lane == 0) {
+#pragma unroll
+      for (int g = 0; g < GC; ++g) {
+        sm.m[warp][g] = m_run[g];
+        sm.l[warp][g] = l_run[g];
+      }
     }
+    if (barrier_or(1, kConsumerWarps * 32, !ok)) break;  // a wait gave up: stop together
+    const int g = threadIdx.x / kD;
+    const int d = threadIdx.x % kD;
+    if (g < GC) {
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm.m[w][g]);
+      float o = 0.f, lse = -INFINITY;
+      if (M != -INFINITY) {
+        float lsum = 0.f, osum = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          const float f = fast_exp2(sm.m[w][g] - M);
+          lsum = fmaf(sm.l[w][g], f, lsum);
+          osum = fmaf(sm.acc[w][g][d], f, osum);
+        }
+        o = osum / lsum;
+        lse = M + log2f(lsum);
+      }
+      const int64_t row = (int64_t)un.b * p.num_q_heads + hq0 + g;
+      if (p.splits == 1) {
+        p.out[row * kD + d] = bf16_bits_rn(o);
+      } else {
+        p.part_o[(row * p.splits + un.s) * kD + d] = o;
+        if (d == 0) p.part_lse[row * p.splits + un.s] = lse;
+      }
+    }
+    named_barrier_sync(2, kConsumerWarps * 32);  // merge buffer free for the next unit
   }
 }
 
@@ -382,9 +456,8 @@ __global__ void __launch_bounds__(128)
 }
 
 template <int GC>
-cudaError_t launch_split(const DecodeArgs &a, const DecodePlan &p, const CUtensorMap &km,
-                         const CUtensorMap &vm, float *part_o, float *part_lse,
-                         cudaStream_t stream) {
+cudaError_t launch_split(const CUtensorMap &km, const CUtensorMap &vm, const DecodeParams &prm,
+                         int num_sms, cudaStream_t stream) {
   const size_t smem = sizeof(DecodeSmem<GC>) + 1024;
   static bool configured[64] = {};
   int dev = 0;
@@ -400,12 +473,8 @@ cudaError_t launch_split(const DecodeArgs &a, const DecodePlan &p, const CUtenso
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  const dim3 grid(a.num_kv_heads * p.head_groups, p.splits, a.batch);
-  const int group = a.num_q_heads / a.num_kv_heads;
-  decode_split_kernel<GC><<<grid, kThreads, smem, stream>>>(
-      km, vm, static_cast<const uint16_t *>(a.q), a.block_tables, a.table_width, a.context_lens,
-      a.num_q_heads, group, p.head_groups, a.block_size, a.num_blocks, p.chunk, p.splits,
-      a.scale * kLog2e, part_o, part_lse, static_cast<uint16_t *>(a.out), a.err);
+  const int64_t ctas = std::min<int64_t>((int64_t)num_sms * 2, prm.units);
+  decode_split_kernel<GC><<<(unsigned)ctas, kThreads, smem, stream>>>(km, vm, prm);
   return cudaGetLastError();
 }
 
@@ -424,8 +493,9 @@ DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
     const int64_t per = (max_ctx + S - 1) / S;
     p.chunk = (int32_t)((per + kTile - 1) / kTile * kTile);
   } else {
-    // Long chunks amortise a CTA's start-up (pipeline fill, q load, merge): take the longest
-    // chunk, up to 16 tiles, that still leaves >= 4 waves of CTAs (two per SM) for balance.
+    // Each unit ends with a merge across the CTA's warps, so long units (up to 16 tiles) pay
+    // off; the work queue balances them as long as there are >= 4 units per CTA slot (two
+    // per SM). Take the longest chunk that keeps that many units.
     const int64_t units = (int64_t)batch * num_kv_heads * p.head_groups;
     const int64_t target = (int64_t)num_sms * 2 * 4;
     int64_t chunk = 16 * kTile;
@@ -433,8 +503,9 @@ DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
     p.chunk = (int32_t)chunk;
   }
   p.splits = (int32_t)((max_ctx + p.chunk - 1) / p.chunk);
-  p.workspace_bytes =
+  const size_t partials =
       p.splits > 1 ? (size_t)batch * num_q_heads * p.splits * (kD + 1) * sizeof(float) : 0;
+  p.workspace_bytes = (partials + 15) / 16 * 16 + kDecodeQueueBytes;  // + the work queue
   return p;
 }
 
@@ -453,16 +524,43 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &p, cudaSt
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
 
-  float *part_o = static_cast<float *>(a.workspace);
-  float *part_lse = part_o ? part_o + (size_t)a.batch * a.num_q_heads * p.splits * kD : nullptr;
-  cudaError_t e = p.heads_per_cta == 2 ? launch_split<2>(a, p, km, vm, part_o, part_lse, stream)
-                                       : launch_split<1>(a, p, km, vm, part_o, part_lse, stream);
+  uint8_t *ws = static_cast<uint8_t *>(a.workspace);
+  const size_t partials = p.workspace_bytes - kDecodeQueueBytes;
+  DecodeParams prm{};
+  prm.q = static_cast<const uint16_t *>(a.q);
+  prm.block_tables = a.block_tables;
+  prm.context_lens = a.context_lens;
+  prm.part_o = p.splits > 1 ? reinterpret_cast<float *>(ws) : nullptr;
+  prm.part_lse = p.splits > 1 ? prm.part_o + (size_t)a.batch * a.num_q_heads * p.splits * kD
+                              : nullptr;
+  prm.out = static_cast<uint16_t *>(a.out);
+  prm.queue = reinterpret_cast<int32_t *>(ws + partials);
+  prm.err = a.err;
+  prm.num_blocks = a.num_blocks;
+  prm.cap = std::min((int64_t)a.table_width * a.block_size, (int64_t)p.splits * p.chunk);
+  prm.table_width = a.table_width;
+  prm.batch = a.batch;
+  prm.num_q_heads = a.num_q_heads;
+  prm.group = a.num_q_heads / a.num_kv_heads;
+  prm.head_groups = p.head_groups;
+  prm.xgroups = a.num_kv_heads * p.head_groups;
+  prm.block_size = a.block_size;
+  prm.chunk = p.chunk;
+  prm.splits = p.splits;
+  const int64_t units = (int64_t)p.splits * a.batch * prm.xgroups;
+  if (units > INT32_MAX) return cudaErrorInvalidValue;
+  prm.units = (int32_t)units;
+  prm.qscale = a.scale * kLog2e;
+
+  cudaError_t e = cudaMemsetAsync(prm.queue, 0, sizeof(int32_t), stream);
+  if (e != cudaSuccess) return e;
+  e = p.heads_per_cta == 2 ? launch_split<2>(km, vm, prm, a.num_sms, stream)
+                           : launch_split<1>(km, vm, prm, a.num_sms, stream);
   if (e != cudaSuccess || p.splits == 1) return e;
   const int64_t rows_out = (int64_t)a.batch * a.num_q_heads;
-  const int64_t cap = std::min((int64_t)a.table_width * a.block_size, (int64_t)p.splits * p.chunk);
   decode_combine_kernel<<<(unsigned)((rows_out + 3) / 4), 128, 0, stream>>>(
-      part_o, part_lse, a.context_lens, a.batch, a.num_q_heads, p.chunk, p.splits, cap,
-      static_cast<uint16_t *>(a.out));
+      prm.part_o, prm.part_lse, a.context_lens, a.batch, a.num_q_heads, p.chunk, p.splits,
+      prm.cap, static_cast<uint16_t *>(a.out));
   return cudaGetLastError();
 }
 

@@ -79,7 +79,8 @@ extern "C" pkv_status pkv_paged_decode_attn_noalloc(
   if (!scratch) return PKV_ERR_CUDA;
   pkv::DecodeArgs a{q,           k_cache,      v_cache,     block_tables, block_table_width,
                     context_lens, batch,        num_q_heads, num_kv_heads, block_size,
-                    num_blocks,  scale,        scratch,     out,          err};
+                    num_blocks,  scale,        scratch,     out,          err,
+                    num_sms};
   return pkv::launch_paged_decode(a, plan, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? PKV_OK
              : PKV_ERR_CUDA;

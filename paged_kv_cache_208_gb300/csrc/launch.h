@@ -44,7 +44,9 @@ struct DecodeArgs {
   void *workspace;
   void *out;
   unsigned int *err;
+  int num_sms;
 };
+constexpr size_t kDecodeQueueBytes = 16;  // the persistent kernel's work counter
 cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &plan,
                                 cudaStream_t stream);
 

@@ -183,12 +183,12 @@ pkv_status pkv_paged_decode_attn(const void *q, const void *k_cache, const void 
   if (!dev) return PKV_ERR_CUDA;
   const pkv::DecodePlan plan = pkv::plan_decode(batch, num_q_heads, num_kv_heads,
                                                 max_context_len, num_splits, dev->num_sms);
-  if (plan.workspace_bytes > 0 &&
-      (!workspace || workspace_bytes < plan.workspace_bytes || !aligned16(workspace)))
+  if (!workspace || workspace_bytes < plan.workspace_bytes || !aligned16(workspace))
     return PKV_ERR_WORKSPACE;
   pkv::DecodeArgs a{q,           k_cache,        v_cache,      block_tables, block_table_width,
                     context_lens, batch,          num_q_heads,  num_kv_heads, block_size,
-                    num_blocks,  scale,          workspace,    out,          dev->err};
+                    num_blocks,  scale,          workspace,    out,          dev->err,
+                    dev->num_sms};
   return launch_status(pkv::launch_paged_decode(a, plan, static_cast<cudaStream_t>(stream)));
 }
 
