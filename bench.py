@@ -41,6 +41,10 @@ B, HQ, HKV, D, BS = 256, w.NUM_Q_HEADS, w.NUM_KV_HEADS, w.HEAD_DIM, w.BLOCK_SIZE
 ROW_BYTES = HKV * D * 2                     # one token's K (or V) row in one layer
 BLOCK_BYTES_ALL_LAYERS = 2 * LAYERS * BS * ROW_BYTES
 FALLBACK_HBM_GBS = 6800.0
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one decode_split_kernel launch on
+# the Qwen3 decode batch, from one ncu capture of the current kernel; None whenever the kernel
+# has changed since that capture.
+DECODE_SPLIT_DRAM_BYTES = 1_184_072_104
 FALLBACK_BF16_TFLOPS = 1900.0
 WORKLOAD = ("qwen3-0.6b decode step: 28 layers x (kv_store of 256 new tokens + paged decode "
             "attention), B=256, ctx U[100,2048] (seed 2), block_size 256, 16 q / 8 kv heads, "
@@ -252,10 +256,13 @@ def time_prefill_store(pkv, iters: int = 20):
             "bytes": nbytes, "l2": "inputs (1.18 GB) larger than L2"}
 
 
-def time_decode_shape(pkv, batch: int, ctx: int, hbm_peak: float, iters: int = 20):
+def time_decode_shape(pkv, batch: int, ctx: int, hbm_peak: float, iters: int = 20,
+                      graph: bool = False):
     """Paged decode attention alone on `batch` sequences of `ctx` tokens (blocks drawn at
     random). Small batches rotate over enough disjoint copies of the pool region that the
-    timed reads (>= 1 GB across the rotation) do not come from L2."""
+    timed reads (>= 1 GB across the rotation) do not come from L2. With `graph`, one CUDA
+    graph holds one call per copy and is replayed, so the time is the GPU's alone (no host
+    call overhead between launches)."""
     per = batch * (-(-ctx // BS))
     reps = max(1, -(-(1 << 30) // (per * BS * ROW_BYTES * 2)))
     lay = w.decode_layout(np.full(batch * reps, ctx, np.int32), per * reps + 8, w.rng(5 + batch))
@@ -267,21 +274,80 @@ def time_decode_shape(pkv, batch: int, ctx: int, hbm_peak: float, iters: int = 2
               for r in range(reps)]
     cl = torch.full((batch,), ctx, dtype=torch.int32, device="cuda")
     ws = pkv.decode_workspace(batch, HQ, HKV, D, ctx, 0)
+    call = lambda r: pkv.paged_decode_attn(q, kc, vc, tables[r], cl, ctx, D ** -0.5,
+                                           workspace=ws, out=out)
     for r in range(min(reps, 3)):
-        pkv.paged_decode_attn(q, kc, vc, tables[r], cl, ctx, D ** -0.5, workspace=ws, out=out)
+        call(r)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    e0.record()
-    for i in range(iters):
-        pkv.paged_decode_attn(q, kc, vc, tables[i % reps], cl, ctx, D ** -0.5, workspace=ws,
-                              out=out)
-    e1.record()
-    torch.cuda.synchronize()
-    t = e0.elapsed_time(e1) / 1e3 / iters
+    if graph:
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                for r in range(reps):
+                    call(r)
+        torch.cuda.current_stream().wait_stream(s)
+        replays = max(1, -(-iters // reps))
+        for _ in range(2):
+            g.replay()
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(replays):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        n = replays * reps
+    else:
+        torch.cuda.synchronize()
+        e0.record()
+        for i in range(iters):
+            call(i % reps)
+        e1.record()
+        torch.cuda.synchronize()
+        n = iters
+    t = e0.elapsed_time(e1) / 1e3 / n
     nbytes = decode_bytes(np.full(batch, ctx), tables[0].shape[1])["decode"]
     del kc, vc
     return {"batch": batch, "ctx": ctx, "us": t * 1e6, "gbs": nbytes / t / 1e9,
-            "frac_of_hbm_peak": nbytes / t / 1e9 / hbm_peak, "kv_tokens_per_s": batch * ctx / t}
+            "frac_of_hbm_peak": nbytes / t / 1e9 / hbm_peak, "kv_tokens_per_s": batch * ctx / t,
+            "timing": "cuda graph replay" if graph else "eager calls"}
+
+
+def time_prefix_prefill(pkv, iters: int = 10):
+    """Prefix-cached prefill: 64 sequences sharing a 2048-token prefix (8 ref-counted blocks)
+    plus private suffixes of U[256, 768] tokens; queries are the suffixes, keys are read
+    through block_table from the pool; one layer timed."""
+    lay = w.prefix_prefill_case_layout(num_blocks=8 + 64 * 3 + 32)
+    kc = w.device_bf16_normal((lay.num_blocks, BS, HKV, D), 701)
+    vc = w.device_bf16_normal((lay.num_blocks, BS, HKV, D), 702)
+    Tq = int(lay.seqlens_q.sum())
+    q = w.device_bf16_normal((Tq, HQ, D), 703)
+    out = torch.empty_like(q)
+    cq = torch.from_numpy(lay.cu_seqlens_q).cuda()
+    ck = torch.from_numpy(lay.cu_seqlens_k).cuda()
+    bt = torch.from_numpy(lay.block_table).cuda()
+    mq, mk = int(lay.seqlens_q.max()), int(lay.seqlens_k.max())
+    call = lambda: pkv.varlen_prefill_attn(q, kc, vc, cq, ck, mq, mk, D ** -0.5, out=out,
+                                           block_table=bt)
+    for _ in range(3):
+        call()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(iters):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / 1e3 / iters
+    Lq = lay.seqlens_q.astype(np.int64)
+    Lk = lay.seqlens_k.astype(np.int64)
+    pairs = int((Lq * (Lk - Lq) + Lq * (Lq + 1) // 2).sum())
+    flops = 4 * HQ * D * pairs
+    return {"tflops": flops / t / 1e12, "ms": t * 1e3, "flops": flops, "causal_pairs": pairs,
+            "query_tokens": Tq, "seqs": int(lay.n),
+            "l2": "the 8 shared prefix blocks (8 MiB of K+V) stay in L2 across sequences"}
 
 
 def time_prefill(pkv, iters: int = 10):
@@ -403,26 +469,42 @@ def run_ours(args):
     extra = {}
     if not args.skip_extra:
         extra["decode_long_context"] = time_decode_shape(pkv, 32, 32768, hbm_peak)
-        extra["decode_batch_sweep"] = [
-            {k: v for k, v in time_decode_shape(pkv, b, 1024, hbm_peak).items()
-             if k in ("batch", "us", "gbs", "frac_of_hbm_peak")}
-            for b in (1, 2, 4, 8, 16, 32, 64, 128, 256, 512)]
+        keep = ("batch", "us", "gbs", "frac_of_hbm_peak")
+        extra["decode_batch_sweep"] = {
+            "ctx": 1024, "timing": "CUDA graph replay of back-to-back calls",
+            "points": [{k: v for k, v in time_decode_shape(pkv, b, 1024, hbm_peak,
+                                                           graph=True).items() if k in keep}
+                       for b in (1, 2, 4, 8, 16, 32, 64, 128, 256, 512)]}
+        extra["decode_batch_sweep"]["first_batch_at_70pct"] = next(
+            (p["batch"] for p in extra["decode_batch_sweep"]["points"]
+             if p["frac_of_hbm_peak"] >= 0.7), None)
+        extra["decode_batch_sweep_eager"] = [
+            {k: v for k, v in time_decode_shape(pkv, b, 1024, hbm_peak).items() if k in keep}
+            for b in (1, 8, 64)]
         extra["kv_store_prefill"] = time_prefill_store(pkv)
         extra["prefill"] = time_prefill(pkv)
         if "tflops" in extra["prefill"]:
             extra["prefill"]["frac_of_bf16_peak"] = extra["prefill"]["tflops"] / bf16_peak
             extra["prefill"]["tflops_x28_layers_ms"] = extra["prefill"]["ms"] * LAYERS
+        extra["prefix_prefill"] = time_prefix_prefill(pkv)
+        extra["prefix_prefill"]["frac_of_bf16_peak"] = extra["prefix_prefill"]["tflops"] / bf16_peak
 
     cpu = None
     if rank == 0 and not args.skip_cpu:
         s = oracle_decode_sample(step, None)
         import oracle
-        t = oracle_step_time(s)
+        # repeat one layer's work until about 10 s of CPU time have run (each repeat writes
+        # the same rows, so the inputs do not change between repeats)
+        reps, total = 0, 0.0
+        while total < 10.0 and reps < 1000:
+            total += oracle_step_time(s)
+            reps += 1
+        t = total / reps
         cpu = {"value": (s["bytes"]["store"] + s["bytes"]["decode"]) / t / 1e9, "unit": "GB/s",
                "cores": oracle.max_threads(), "kind": "oracle",
-               "sample": "one layer (of 28) of the full batch: kv_store + paged decode of all "
-                         "256 sequences, fp64 C oracle with OpenMP",
-               "seconds": t}
+               "sample": f"one layer (of 28) of the full batch, repeated {reps} times: kv_store "
+                         "+ paged decode of all 256 sequences, fp64 C oracle with OpenMP",
+               "seconds": total}
     if rank != 0:
         return
     total_bytes = step.step_bytes * world
@@ -451,7 +533,9 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "kernel": "paged_decode_attn (split + combine)",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "peak_source": peak_src,
-                     "traffic": None, "algorithmic_bytes_per_launch": dec_bytes,
+                     "traffic": DECODE_SPLIT_DRAM_BYTES,
+                     "traffic_kernel": "decode_split_kernel (ncu, one launch, same workload)",
+                     "algorithmic_bytes_per_launch": dec_bytes,
                      "avg_launch_us": decode_avg * 1e6},
         "e2e": {"value": total_bytes / e2e_dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_dt * 1e3},
@@ -504,7 +588,8 @@ def run_reference(args):
 def run_profile(args):
     """One kernel alone on its workload, for ncu: `decode` (the Qwen3 batch, one layer, a pool
     of just the referenced blocks: 1.2 GB, larger than L2), `prefill` (the varlen workload,
-    packed) or `store` (the varlen workload's kv_store). Runs --warmup + --steps launches."""
+    packed), `prefix` (the prefix-cached workload, keys through block_table) or `store` (the
+    varlen workload's kv_store). Runs --warmup + --steps launches."""
     torch.cuda.set_device(0)
     pkv = load_pkv()
     if args.profile == "decode":
@@ -525,6 +610,18 @@ def run_profile(args):
         vc = torch.empty_like(kc)
         slots = torch.from_numpy(lay.slot_mapping).cuda()
         run = lambda: pkv.kv_store(k, v, slots, kc, vc)
+    elif args.profile == "prefix":
+        lay = w.prefix_prefill_case_layout(num_blocks=8 + 64 * 3 + 32)
+        kc = w.device_bf16_normal((lay.num_blocks, BS, HKV, D), 701)
+        vc = w.device_bf16_normal((lay.num_blocks, BS, HKV, D), 702)
+        q = w.device_bf16_normal((int(lay.seqlens_q.sum()), HQ, D), 703)
+        out = torch.empty_like(q)
+        cq = torch.from_numpy(lay.cu_seqlens_q).cuda()
+        ck = torch.from_numpy(lay.cu_seqlens_k).cuda()
+        bt = torch.from_numpy(lay.block_table).cuda()
+        mq, mk = int(lay.seqlens_q.max()), int(lay.seqlens_k.max())
+        run = lambda: pkv.varlen_prefill_attn(q, kc, vc, cq, ck, mq, mk, D ** -0.5, out=out,
+                                              block_table=bt)
     else:
         lens = w.varlen_prefill_lengths()
         cu = torch.from_numpy(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)).cuda()
@@ -557,7 +654,7 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--num-splits", type=int, default=0,
                     help="decode KV splits of the longest context (0 = the library's choice)")
-    ap.add_argument("--profile", choices=["decode", "prefill", "store"],
+    ap.add_argument("--profile", choices=["decode", "prefill", "prefix", "store"],
                     help="run one kernel alone (for ncu); prints no benchmark line")
     args = ap.parse_args()
     if args.warmup < 3:
