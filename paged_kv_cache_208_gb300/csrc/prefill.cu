@@ -167,12 +167,14 @@ __device__ __forceinline__ Item decode_item(const PrefillParams &p, int i) {
   return it;
 }
 
-// Next work item from the ring (in order). it.id < 0 at the end of the work, or when the
-// wait gave up. The caller releases the slot (item_empty) after copying the item.
+// Next work item from the ring (in order), taken by a whole warp: every lane waits, and the
+// item counts only if every lane saw it (so the warp agrees even when a wait gives up).
+// it.id < 0 at the end of the work, or when the wait gave up. The caller releases the slot
+// (item_empty) after copying the item.
 __device__ __forceinline__ Item take_item(PrefillSmem &sm, uint32_t taken, unsigned int *err) {
   const int slot = taken % kRing;
   Item it;
-  if (wait_parity(&sm.item_full[slot], (taken / kRing) & 1, err)) {
+  if (__all_sync(0xffffffffu, wait_parity(&sm.item_full[slot], (taken / kRing) & 1, err))) {
     it = sm.items[slot];
   } else {
     it.id = -1;
@@ -180,25 +182,40 @@ __device__ __forceinline__ Item take_item(PrefillSmem &sm, uint32_t taken, unsig
   return it;
 }
 
-// S = Q K^T for one 128 x 128 tile: 8 UMMAs of K = 16 over the two 64-column halves.
-__device__ __forceinline__ void mma_qk(uint32_t d_tmem, uint32_t q_addr, uint32_t k_addr,
+// S = Q K^T for one 128 x 128 tile: 8 UMMAs of K = 16 over the two 64-column halves. The
+// descriptors are the tiles' base descriptors plus compile-time offsets (the start address
+// sits in the low bits, in 16-byte units). Called by the whole MMA warp; one lane issues.
+__device__ __forceinline__ void mma_qk(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc,
                                        uint32_t idesc) {
+  if (elect_one()) {
+    umma_ss<false>(d_tmem, q_desc, k_desc, idesc);
 #pragma unroll
-  for (int kk = 0; kk < kD / 16; ++kk) {
-    const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-    umma_bf16(d_tmem, smem_desc_sw128(q_addr + off, 16, 1024),
-              smem_desc_sw128(k_addr + off, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+    for (int kk = 1; kk < kD / 16; ++kk) {
+      const uint64_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+      umma_ss<true>(d_tmem, q_desc + off, k_desc + off, idesc);
+    }
   }
+  __syncwarp();
 }
 
-// O (+)= P V for one tile: P from TMEM (8 columns per 16 keys), V MN-major in smem.
-__device__ __forceinline__ void mma_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_addr,
+// O (+)= P V for one tile: P from TMEM (8 columns per 16 keys), V MN-major in smem (16 keys
+// = 2 KiB further per step).
+__device__ __forceinline__ void mma_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc,
                                        uint32_t idesc, bool accumulate) {
+  if (elect_one()) {
+    if (accumulate) umma_ts<true>(d_tmem, p_tmem, v_desc, idesc);
+    else umma_ts<false>(d_tmem, p_tmem, v_desc, idesc);
 #pragma unroll
-  for (int kk = 0; kk < kBN / 16; ++kk)
-    umma_bf16_tmem_a(d_tmem, p_tmem + 8 * kk,
-                     smem_desc_sw128(v_addr + kk * 16 * 128, kHalfBytes, 1024), idesc,
-                     (accumulate || kk > 0) ? 1u : 0u);
+    for (int kk = 1; kk < kBN / 16; ++kk)
+      umma_ts<true>(d_tmem, p_tmem + 8 * kk, v_desc + ((kk * 16 * 128) >> 4), idesc);
+  }
+  __syncwarp();
+}
+
+// tcgen05.commit from the lane that issued the UMMAs (the warp is converged here too).
+__device__ __forceinline__ void commit_one(uint64_t *bar) {
+  if (elect_one()) umma_commit(bar);
+  __syncwarp();
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -247,9 +264,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = sm.tmem_base;
-
-  // Consumers take item ids from the ring in order; every slot is released by the MMA thread
-  // and the 8 softmax warps. Returns -1 at the end of the work (or when a wait gave up).
 
   // Register split (launch: kLaunchRegs x 384 threads): the two softmax warpgroups hold a
   // whole 128-column S row per thread; warpgroup 2 only schedules, loads and issues MMAs.
@@ -375,89 +389,96 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ UMMA issuer
-    if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_bf16_f32(kBM, kBN, 0, 0);  // Q (K-major) x K (K-major)
-      constexpr uint32_t kIdO = idesc_bf16_f32(kBM, kD, 0, 1);   // P (TMEM) x V (MN-major)
-      const uint32_t qa0 = smem_addr(sm.q[0]), qa1 = smem_addr(sm.q[1]);
-      const uint32_t kv0 = smem_addr(sm.kv[0]);
-      uint32_t taken = 0, q_loads = 0, g = 0;
-      uint32_t fix_parity = 0;  // bit s: parity of the next v_fixed phase of slot s
-      bool ok = true;
-      // V(j) of tile gg: wait for the load (or, for a fixed last tile, for the fix)
-      auto v_ready = [&](uint32_t gg, bool fixed) -> bool {
-        const uint32_t n = 2 * gg + 1, vs = n % kSlots;
-        if (fixed) {
-          const bool r = wait_parity(&sm.v_fixed[vs], (fix_parity >> vs) & 1, p.err);
-          fix_parity ^= 1u << vs;
-          return r;
-        }
-        return wait_parity(&sm.kv_full[vs], (n / kSlots) & 1, p.err);
-      };
-      while (ok) {
-        const Item it = take_item(sm, taken, p.err);
-        mbar_arrive(&sm.item_empty[taken % kRing]);
-        ++taken;
-        if (it.id < 0) break;
-        if (it.nk == 0) continue;
-        const int nk = it.nk;
-        const bool fix_v = it.last_rows < kBN;
-        for (int j = 0; j < nk; ++j, ++g) {
-          const uint32_t ks = (2 * g) % kSlots;
-          const uint32_t ka = kv0 + ks * kTileBytes;
-          ok = wait_parity(&sm.kv_full[ks], ((2 * g) / kSlots) & 1, p.err);
-          if (!ok) break;
-          tc_fence_after_sync();
-          // S_0(j)
-          if (j == 0) {
-            ok = wait_parity(&sm.q_full[0], q_loads & 1, p.err);
-            if (!ok) break;
-            tc_fence_after_sync();
-          }
-          mma_qk(tmem, qa0, ka, kIdS);
-          umma_commit(&sm.s_full[0]);
-          if (j == nk - 1) umma_commit(&sm.q_empty[0]);
-          // O_1 += P_1(j-1) V(j-1)  (never the last tile here)
-          if (j > 0) {
-            const uint32_t gp = g - 1, vs = (2 * gp + 1) % kSlots;
-            ok = wait_parity(&sm.p_full[1], gp & 1, p.err) && v_ready(gp, false);
-            if (!ok) break;
-            tc_fence_after_sync();
-            mma_pv(tmem + 384, tmem + 128, kv0 + vs * kTileBytes, kIdO, j - 1 > 0);
-            umma_commit(&sm.o_full[1]);
-            umma_commit(&sm.kv_empty[vs]);
-          }
-          // S_1(j)
-          if (j == 0) {
-            ok = wait_parity(&sm.q_full[1], q_loads & 1, p.err);
-            if (!ok) break;
-            tc_fence_after_sync();
-          }
-          mma_qk(tmem + 128, qa1, ka, kIdS);
-          umma_commit(&sm.s_full[1]);
-          if (j == nk - 1) umma_commit(&sm.q_empty[1]);
-          umma_commit(&sm.kv_empty[ks]);
-          // O_0 += P_0(j) V(j); for a fixed last tile this wait also covers O_1's use below
-          ok = wait_parity(&sm.p_full[0], g & 1, p.err) && v_ready(g, j == nk - 1 && fix_v);
-          if (!ok) break;
-          tc_fence_after_sync();
-          mma_pv(tmem + 256, tmem, kv0 + ((2 * g + 1) % kSlots) * kTileBytes, kIdO, j > 0);
-          umma_commit(&sm.o_full[0]);
-        }
-        if (!ok) break;
-        {  // O_1 += P_1(last) V(last): V(last) is ready (waited above)
-          const uint32_t gp = g - 1, vs = (2 * gp + 1) % kSlots;
-          ok = wait_parity(&sm.p_full[1], gp & 1, p.err);
-          if (!ok) break;
-          tc_fence_after_sync();
-          mma_pv(tmem + 384, tmem + 128, kv0 + vs * kTileBytes, kIdO, nk > 1);
-          umma_commit(&sm.o_full[1]);
-          umma_commit(&sm.kv_empty[vs]);
-        }
-        ++q_loads;
+    // The whole warp runs this loop (waits, descriptor arithmetic) so that it stays
+    // converged; one elected lane issues each group of UMMAs and its commits.
+    constexpr uint32_t kIdS = idesc_bf16_f32(kBM, kBN, 0, 0);  // Q (K-major) x K (K-major)
+    constexpr uint32_t kIdO = idesc_bf16_f32(kBM, kD, 0, 1);   // P (TMEM) x V (MN-major)
+    constexpr uint64_t kSlotStep = kTileBytes >> 4;            // one ring slot, descriptor units
+    const uint64_t dq0 = smem_desc_sw128(smem_addr(sm.q[0]), 16, 1024);
+    const uint64_t dq1 = smem_desc_sw128(smem_addr(sm.q[1]), 16, 1024);
+    const uint64_t dk0 = smem_desc_sw128(smem_addr(sm.kv[0]), 16, 1024);
+    const uint64_t dv0 = smem_desc_sw128(smem_addr(sm.kv[0]), kHalfBytes, 1024);
+    uint32_t taken = 0, q_loads = 0, g = 0;
+    uint32_t fix_parity = 0;  // bit s: parity of the next v_fixed phase of slot s
+    bool ok = true;
+    // warp-uniform wait
+    auto wait_all = [&](uint64_t *bar, uint32_t parity) -> bool {
+      return __all_sync(kFull, wait_parity(bar, parity, p.err));
+    };
+    // V(j) of tile gg: wait for the load (or, for a fixed last tile, for the fix)
+    auto v_ready = [&](uint32_t gg, bool fixed) -> bool {
+      const uint32_t n = 2 * gg + 1, vs = n % kSlots;
+      if (fixed) {
+        const bool r = wait_all(&sm.v_fixed[vs], (fix_parity >> vs) & 1);
+        fix_parity ^= 1u << vs;
+        return r;
       }
-      // every UMMA must be complete before the tensor memory is released
-      if (ok && g > 0) wait_parity(&sm.o_full[1], (g - 1) & 1, p.err);
+      return wait_all(&sm.kv_full[vs], (n / kSlots) & 1);
+    };
+    while (ok) {
+      Item it = take_item(sm, taken, p.err);
+      __syncwarp();  // every lane has copied the item before the slot is released
+      if (lane == 0) mbar_arrive(&sm.item_empty[taken % kRing]);
+      ++taken;
+      if (it.id < 0) break;
+      if (it.nk == 0) continue;
+      const int nk = it.nk;
+      const bool fix_v = it.last_rows < kBN;
+      for (int j = 0; j < nk; ++j, ++g) {
+        const uint32_t ks = (2 * g) % kSlots;
+        ok = wait_all(&sm.kv_full[ks], ((2 * g) / kSlots) & 1);
+        if (!ok) break;
+        tc_fence_after_sync();
+        // S_0(j)
+        if (j == 0) {
+          ok = wait_all(&sm.q_full[0], q_loads & 1);
+          if (!ok) break;
+          tc_fence_after_sync();
+        }
+        mma_qk(tmem, dq0, dk0 + ks * kSlotStep, kIdS);
+        commit_one(&sm.s_full[0]);
+        if (j == nk - 1) commit_one(&sm.q_empty[0]);
+        // O_1 += P_1(j-1) V(j-1)  (never the last tile here)
+        if (j > 0) {
+          const uint32_t gp = g - 1, vs = (2 * gp + 1) % kSlots;
+          ok = wait_all(&sm.p_full[1], gp & 1) && v_ready(gp, false);
+          if (!ok) break;
+          tc_fence_after_sync();
+          mma_pv(tmem + 384, tmem + 128, dv0 + vs * kSlotStep, kIdO, j - 1 > 0);
+          commit_one(&sm.o_full[1]);
+          commit_one(&sm.kv_empty[vs]);
+        }
+        // S_1(j)
+        if (j == 0) {
+          ok = wait_all(&sm.q_full[1], q_loads & 1);
+          if (!ok) break;
+          tc_fence_after_sync();
+        }
+        mma_qk(tmem + 128, dq1, dk0 + ks * kSlotStep, kIdS);
+        commit_one(&sm.s_full[1]);
+        if (j == nk - 1) commit_one(&sm.q_empty[1]);
+        commit_one(&sm.kv_empty[ks]);
+        // O_0 += P_0(j) V(j); for a fixed last tile this wait also covers O_1's use below
+        ok = wait_all(&sm.p_full[0], g & 1) && v_ready(g, j == nk - 1 && fix_v);
+        if (!ok) break;
+        tc_fence_after_sync();
+        mma_pv(tmem + 256, tmem, dv0 + ((2 * g + 1) % kSlots) * kSlotStep, kIdO, j > 0);
+        commit_one(&sm.o_full[0]);
+      }
+      if (!ok) break;
+      {  // O_1 += P_1(last) V(last): V(last) is ready (waited above)
+        const uint32_t gp = g - 1, vs = (2 * gp + 1) % kSlots;
+        ok = wait_all(&sm.p_full[1], gp & 1);
+        if (!ok) break;
+        tc_fence_after_sync();
+        mma_pv(tmem + 384, tmem + 128, dv0 + vs * kSlotStep, kIdO, nk > 1);
+        commit_one(&sm.o_full[1]);
+        commit_one(&sm.kv_empty[vs]);
+      }
+      ++q_loads;
     }
+    // every UMMA must be complete before the tensor memory is released
+    if (ok && g > 0) wait_all(&sm.o_full[1], (g - 1) & 1);
   }
   } else {
     reg_alloc_inc<kSoftmaxRegs>();
@@ -471,8 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     while (ok) {
       Item it = take_item(sm, taken, p.err);
-      it.id = __shfl_sync(kFull, it.id, 0);  // warp-uniform end / give-up decision
-      __syncwarp();
+      __syncwarp();  // every lane has copied the item before the slot is released
       if (lane == 0) mbar_arrive(&sm.item_empty[taken % kRing]);
       ++taken;
       if (it.id < 0) break;
