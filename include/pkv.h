@@ -154,9 +154,13 @@ pkv_status pkv_paged_decode_attn(const void *q, const void *k_cache, const void 
                                  void *stream);
 
 /*
- * Bytes of device workspace that pkv_varlen_prefill_attn needs: 16 for every size (the
- * persistent kernel's work counter, which the call resets on its stream before the kernel
- * runs). Returns 0 for invalid sizes.
+ * Bytes of device workspace that pkv_varlen_prefill_attn needs for num_seqs sequences of at
+ * most max_seqlen_q queries: a 16-byte header (the persistent kernel's work counter and the
+ * length of its work list), about 12 bytes per sequence and 8 per possible query-block count
+ * for sorting, and the work list itself, 8 bytes per (sequence, 128-query block):
+ * about 16 + 12 * num_seqs + 8 * num_seqs * ceil(max_seqlen_q / 128). The call writes all of
+ * it on its stream before the attention kernel runs, so its contents need no initialisation.
+ * Returns 0 for invalid sizes, or when the list would exceed 2^31 - 1 entries.
  */
 size_t pkv_prefill_workspace_bytes(int32_t num_seqs, int32_t max_seqlen_q,
                                    int32_t num_q_heads, int32_t head_dim);

@@ -73,10 +73,34 @@ struct PrefillArgs {
   float scale;
   int32_t causal;
   void *out;
-  void *workspace;   // kPrefillWorkspaceBytes: the persistent kernel's work counter
+  void *workspace;   // prefill_workspace_layout(...).bytes: the work list and its counter
   unsigned int *err;
 };
-constexpr size_t kPrefillWorkspaceBytes = 16;
+
+// The prefill workspace: a 16-byte header (work counter, number of work units), the
+// per-sequence query-block counts, the sequences ranked by that count, the first unit of each
+// ranked sequence, two histograms over the counts, and the unit list itself -- one
+// (sequence, query block) pair per unit, at most num_seqs * ceil(max_seqlen_q / 128).
+struct PrefillWorkspace {
+  size_t counts, ranked, unit_start, hist, fill, units, bytes;
+  int64_t max_units;
+  int32_t levels;  // ceil(max_seqlen_q / 128): the query blocks of the longest sequence
+};
+inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
+inline PrefillWorkspace prefill_workspace_layout(int32_t num_seqs, int32_t max_seqlen_q) {
+  PrefillWorkspace w{};
+  w.levels = (int32_t)(((int64_t)max_seqlen_q + 127) / 128);
+  w.max_units = (int64_t)num_seqs * w.levels;
+  const size_t n = (size_t)num_seqs, l = (size_t)w.levels + 1;
+  w.counts = 16;
+  w.ranked = align16(w.counts + 4 * n);
+  w.unit_start = align16(w.ranked + 4 * n);
+  w.hist = align16(w.unit_start + 4 * (n + 1));
+  w.fill = align16(w.hist + 4 * l);
+  w.units = align16(w.fill + 4 * l);
+  w.bytes = align16(w.units + 8 * (size_t)w.max_units);
+  return w;
+}
 cudaError_t launch_varlen_prefill(const PrefillArgs &a, int num_sms, cudaStream_t stream);
 bool prefill_group_supported(int group);  // num_q_heads / num_kv_heads
 

@@ -195,7 +195,9 @@ pkv_status pkv_paged_decode_attn(const void *q, const void *k_cache, const void 
 size_t pkv_prefill_workspace_bytes(int32_t num_seqs, int32_t max_seqlen_q, int32_t num_q_heads,
                                    int32_t head_dim) {
   if (num_seqs < 0 || max_seqlen_q < 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
-  return pkv::kPrefillWorkspaceBytes;
+  const pkv::PrefillWorkspace w = pkv::prefill_workspace_layout(num_seqs, max_seqlen_q);
+  if (w.max_units > INT32_MAX) return 0;
+  return w.bytes;
 }
 
 pkv_status pkv_varlen_prefill_attn(const void *q, int64_t q_tok_stride, int64_t total_q,
@@ -229,7 +231,9 @@ pkv_status pkv_varlen_prefill_attn(const void *q, int64_t q_tok_stride, int64_t 
   if (q_tok_stride % 8 != 0 || kv_tok_stride % 8 != 0 || !aligned16(q) || !aligned16(k) ||
       !aligned16(v) || !aligned16(out))
     return PKV_ERR_UNSUPPORTED;
-  if (!workspace || workspace_bytes < pkv::kPrefillWorkspaceBytes || !aligned16(workspace))
+  const pkv::PrefillWorkspace wl = pkv::prefill_workspace_layout(num_seqs, max_seqlen_q);
+  if (wl.max_units > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < wl.bytes || !aligned16(workspace))
     return PKV_ERR_WORKSPACE;
   DeviceInfo *dev = device_info();
   if (!dev) return PKV_ERR_CUDA;

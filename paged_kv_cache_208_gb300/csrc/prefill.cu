@@ -5,10 +5,14 @@
 // table (prefix caching: queries cover only the uncached suffix and the causal mask is
 // aligned to the end of the keys).
 //
-// Persistent kernel: one CTA per SM takes work items from a global queue (one atomic counter
-// in the caller's workspace; items ordered longest first, so the queue balances the SMs). The
-// producer warp takes the items and hands their ids to the other warps through a small ring
-// in shared memory. An item is
+// Persistent kernel: one CTA per SM takes work items from a global queue (an atomic counter
+// in the caller's workspace). A one-CTA planning kernel first writes the work list there:
+// only (sequence, query block) units that have queries, sequences with the most query blocks
+// first and each sequence's blocks heaviest first, all heads of a unit next to each other.
+// The heavy work starts first (the queue balances the SMs), and the query blocks of one
+// sequence run at about the same time, so the K/V tiles they share come from L2. The
+// producer warp takes the items and hands them to the other warps through a small ring in
+// shared memory. An item is
 // one sequence n, one KV head h and two 128-row M-tiles that share every K/V tile: for a GQA
 // group of two (or a pair of heads of a larger group) the two query heads over the same 128
 // tokens; without GQA two consecutive 128-token blocks of the one head. Per 128-key tile j:
@@ -106,8 +110,8 @@ struct PrefillParams {
   int32_t num_seqs;
   int32_t num_q_heads;
   int32_t num_kv_heads;
-  int32_t qblocks;  // query blocks of one item (128 tokens with GQA pairs, 256 without)
-  int32_t items;
+  const int2 *units;        // work list: (sequence, query block), written by the planner
+  const int32_t *num_units; // its length (written by the planner)
   float scale_log2;
   int32_t causal;
   uint16_t *out;
@@ -116,18 +120,17 @@ struct PrefillParams {
 };
 
 
-// Item i of the walk. Items are ordered by query block, last block first, so the tiles with
-// the most keys start first; every role decodes the same sequence of items.
+// Item i of the work list: unit i / (KV heads x head pairs), head pair i % that.
 template <int G>
 __device__ __forceinline__ Item decode_item(const PrefillParams &p, int i) {
   constexpr int kPairs = G >= 2 ? G / 2 : 1;
   Item it;
   it.id = i;
-  const int per_qb = p.num_seqs * p.num_kv_heads * kPairs;
-  const int qb = p.qblocks - 1 - i / per_qb;
-  const int r = i % per_qb;
-  it.n = r / (p.num_kv_heads * kPairs);
-  const int hp = r % (p.num_kv_heads * kPairs);
+  const int per_unit = p.num_kv_heads * kPairs;
+  const int2 u = p.units[i / per_unit];
+  const int hp = i % per_unit;
+  const int qb = u.y;
+  it.n = u.x;
   it.h = hp / kPairs;
   const int pair = hp % kPairs;
   if (G >= 2) {
@@ -283,6 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t pushed = 0, q_loads = 0, g = 0;
     int last_load = -1;
     bool ok = true;
+    const int total_items = lane == 0 ? *p.num_units * p.num_kv_heads * (G >= 2 ? G / 2 : 1) : 0;
     while (ok) {
       // take the next item that has queries; -1 when the queue is exhausted
       int i = -1;
@@ -291,12 +295,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         d.id = -1;
         while (true) {
           i = atomicAdd(p.queue, 1);
-          if (i >= p.items) break;
+          if (i >= total_items) break;
           d = decode_item<G>(p, i);
           if (d.bad) record_error(p.err, 8u /* SEQLEN_RANGE */);
           if (d.valid) break;
         }
-        if (i >= p.items) {
+        if (i >= total_items) {
           i = -1;
           d.id = -1;
         }
@@ -621,6 +625,110 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------- work-list planner
+struct PlanParams {
+  const int32_t *cu_q;
+  int32_t num_seqs;
+  int32_t levels;           // most query blocks a sequence may have
+  int32_t tokens_per_unit;  // query rows of one unit (128, or 256 without GQA pairs)
+  int64_t total_q;
+  int32_t *header;          // [0] work counter, [1] number of units
+  int32_t *counts, *ranked, *unit_start, *hist, *fill;
+  int2 *units;
+  unsigned int *err;
+};
+constexpr int kPlanThreads = 1024;
+
+// Exclusive prefix sum of one value per thread over the block; `total` gets the block's sum.
+__device__ __forceinline__ int block_exclusive_scan(int v, int *warp_sums, int &total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_sums[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFull, w, o);
+      if (lane >= o) w += y;
+    }
+    warp_sums[lane] = w;
+  }
+  __syncthreads();
+  const int base = warp > 0 ? warp_sums[warp - 1] : 0;
+  total = warp_sums[31];
+  __syncthreads();  // warp_sums is reused by the next call
+  return base + x - v;
+}
+
+// One CTA: count each sequence's query blocks, rank the sequences by that count (most first;
+// a counting sort), and write the unit list. Sequences whose cu_seqlens_q are inconsistent
+// get no units and set PKV_DEVERR_SEQLEN_RANGE, as does a sequence longer than the host's
+// max_seqlen_q (its blocks past that bound are dropped).
+__global__ void __launch_bounds__(kPlanThreads, 1) prefill_plan_kernel(const PlanParams p) {
+  __shared__ int warp_sums[32];
+  const int tid = threadIdx.x;
+  for (int c = tid; c <= p.levels; c += kPlanThreads) {
+    p.hist[c] = 0;
+    p.fill[c] = 0;
+  }
+  __syncthreads();
+  for (int n = tid; n < p.num_seqs; n += kPlanThreads) {
+    const int64_t a = p.cu_q[n], b = p.cu_q[n + 1];
+    int c = 0;
+    if (a < 0 || b < a || b > p.total_q) {
+      record_error(p.err, 8u /* SEQLEN_RANGE */);
+    } else {
+      const int64_t cc = (b - a + p.tokens_per_unit - 1) / p.tokens_per_unit;
+      if (cc > p.levels) record_error(p.err, 8u /* SEQLEN_RANGE */);
+      c = (int)min(cc, (int64_t)p.levels);
+    }
+    p.counts[n] = c;
+    atomicAdd(&p.hist[c], 1);
+  }
+  __syncthreads();
+  // first rank of each count: the sequences with a larger count come before it
+  int carry = 0;
+  for (int r0 = 0; r0 <= p.levels; r0 += kPlanThreads) {
+    const int r = r0 + tid, c = p.levels - r;
+    int total;
+    const int ex = block_exclusive_scan(r <= p.levels ? p.hist[c] : 0, warp_sums, total);
+    if (r <= p.levels) p.fill[c] = carry + ex;
+    carry += total;
+  }
+  __syncthreads();
+  for (int n = tid; n < p.num_seqs; n += kPlanThreads)
+    p.ranked[atomicAdd(&p.fill[p.counts[n]], 1)] = n;
+  __syncthreads();
+  // first unit of each ranked sequence
+  carry = 0;
+  for (int k0 = 0; k0 < p.num_seqs; k0 += kPlanThreads) {
+    const int k = k0 + tid;
+    int total;
+    const int ex = block_exclusive_scan(k < p.num_seqs ? p.counts[p.ranked[k]] : 0, warp_sums,
+                                        total);
+    if (k < p.num_seqs) p.unit_start[k] = carry + ex;
+    carry += total;
+  }
+  __syncthreads();
+  // the units of each ranked sequence, its last query block first
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int k = warp; k < p.num_seqs; k += kPlanThreads / 32) {
+    const int n = p.ranked[k], c = p.counts[n], base = p.unit_start[k];
+    for (int u = lane; u < c; u += 32) p.units[base + u] = make_int2(n, c - 1 - u);
+  }
+  if (tid == 0) {
+    p.unit_start[p.num_seqs] = carry;
+    p.header[0] = 0;
+    p.header[1] = carry;
+  }
+}
+
 template <int G>
 cudaError_t launch_g(const PrefillArgs &a, PrefillParams prm, int num_sms, cudaStream_t stream) {
   constexpr int kPairs = G >= 2 ? G / 2 : 1;
@@ -660,14 +768,31 @@ cudaError_t launch_g(const PrefillArgs &a, PrefillParams prm, int num_sms, cudaS
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  prm.qblocks = (a.max_seqlen_q + kTokensPerItem - 1) / kTokensPerItem;
-  prm.queue = static_cast<int32_t *>(a.workspace);
-  const int64_t items = (int64_t)prm.qblocks * a.num_seqs * a.num_kv_heads * kPairs;
+  const PrefillWorkspace wl = prefill_workspace_layout(a.num_seqs, a.max_seqlen_q);
+  uint8_t *ws = static_cast<uint8_t *>(a.workspace);
+  PlanParams pp{};
+  pp.cu_q = a.cu_seqlens_q;
+  pp.num_seqs = a.num_seqs;
+  pp.levels = wl.levels;
+  pp.tokens_per_unit = kTokensPerItem;
+  pp.total_q = a.total_q;
+  pp.header = reinterpret_cast<int32_t *>(ws);
+  pp.counts = reinterpret_cast<int32_t *>(ws + wl.counts);
+  pp.ranked = reinterpret_cast<int32_t *>(ws + wl.ranked);
+  pp.unit_start = reinterpret_cast<int32_t *>(ws + wl.unit_start);
+  pp.hist = reinterpret_cast<int32_t *>(ws + wl.hist);
+  pp.fill = reinterpret_cast<int32_t *>(ws + wl.fill);
+  pp.units = reinterpret_cast<int2 *>(ws + wl.units);
+  pp.err = a.err;
+  prm.queue = pp.header;
+  prm.num_units = pp.header + 1;
+  prm.units = pp.units;
+  const int64_t items = wl.max_units * a.num_kv_heads * kPairs;  // an upper bound
   if (items <= 0) return cudaSuccess;
   if (items > INT32_MAX) return cudaErrorInvalidValue;
-  prm.items = (int32_t)items;
   const unsigned grid = (unsigned)(items < num_sms ? items : num_sms);
-  cudaError_t e = cudaMemsetAsync(a.workspace, 0, kPrefillWorkspaceBytes, stream);
+  prefill_plan_kernel<<<1, kPlanThreads, 0, stream>>>(pp);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   prefill_kernel<G><<<grid, kThreads, smem, stream>>>(qm, km, vm, prm);
   return cudaGetLastError();

@@ -70,7 +70,7 @@ def test_decode_argument_checks():
 def _prefill(**kw):
     a = dict(q=FAKE, qs=2048, tq=100, k=FAKE, v=FAKE, kvs=1024, tk=100, cq=FAKE, ck=FAKE, N=2,
              mq=64, mk=64, bt=None, W=0, bs=0, nb=0, hq=16, hkv=8, d=128, scale=0.088, causal=1,
-             ws=FAKE, wsb=16, out=FAKE)
+             ws=FAKE, wsb=1 << 20, out=FAKE)
     a.update(kw)
     return L.pkv_varlen_prefill_attn(a["q"], a["qs"], a["tq"], a["k"], a["v"], a["kvs"], a["tk"],
                                      a["cq"], a["ck"], a["N"], a["mq"], a["mk"], a["bt"], a["W"],
@@ -92,14 +92,21 @@ def test_prefill_argument_checks():
     assert _prefill(qs=2052) == pkv.ERR_UNSUPPORTED                # stride not 16-byte multiple
     assert _prefill(ws=None) == pkv.ERR_WORKSPACE
     assert _prefill(wsb=8) == pkv.ERR_WORKSPACE
+    need = L.pkv_prefill_workspace_bytes(2, 64, 16, 128)
+    assert _prefill(wsb=need - 16) == pkv.ERR_WORKSPACE            # the work list does not fit
 
 
 def test_workspace_query_without_device_is_zero_or_sized():
     n = L.pkv_decode_workspace_bytes(4, 16, 8, 128, 300, 0)
     assert n == 0 or n >= 16   # 0 without a device to plan for
     assert L.pkv_decode_workspace_bytes(4, 16, 8, 64, 300, 0) == 0
-    assert L.pkv_prefill_workspace_bytes(4, 100, 16, 128) == 16
+    # a header and sort arrays, then one 8-byte unit per (sequence, 128-query block) at most
+    for n, L_q in ((4, 100), (256, 1024), (1, 131072), (0, 0)):
+        b = L.pkv_prefill_workspace_bytes(n, L_q, 16, 128)
+        assert b % 16 == 0 and b >= 16 + 8 * n * (-(-L_q // 128)), (n, L_q, b)
+        assert b <= 16 + 8 * n * (-(-L_q // 128)) + 32 * (n + 1) + 16 * (-(-L_q // 128) + 1) + 96
     assert L.pkv_prefill_workspace_bytes(-1, 100, 16, 128) == 0
+    assert L.pkv_prefill_workspace_bytes(100000, 2 ** 30, 16, 128) == 0   # list too long
 
 
 def test_product_path_has_no_oracle_import():

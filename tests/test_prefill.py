@@ -175,6 +175,31 @@ def test_prefill_bad_block_id_is_flagged():
     assert pkv.get_device_errors() & pkv.DEVERR_BLOCK_RANGE
 
 
+def test_prefill_skewed_lengths():
+    """One long prompt among many one- to three-token ones: the work list holds only blocks
+    that have queries (the long prompt's 20 blocks first), and every row matches the oracle."""
+    lens = [2500] + [1, 2, 3] * 40
+    q, k, v, cq, ck = _case(lens, seed=29)
+    ref = oracle.varlen_prefill(q, k, v, cq, ck, 128 ** -0.5)
+    pkv.get_device_errors(reset=True)
+    assert_attention_close(_run(q, k, v, cq, ck), ref, "skewed")
+    assert pkv.get_device_errors() == 0
+
+
+def test_prefill_longer_than_max_seqlen_is_flagged():
+    """A sequence longer than max_seqlen_q sets the sequence-length error bit (its query
+    blocks past the bound are not computed); the other sequences are unaffected."""
+    lens = [100, 300]
+    q, k, v, cq, ck = _case(lens, seed=31)
+    ref = oracle.varlen_prefill(q, k, v, cq, ck, 128 ** -0.5)
+    pkv.get_device_errors(reset=True)
+    out = pkv.varlen_prefill_attn(dev(q), dev(k), dev(v), dev(cq), dev(ck), 128, 300,
+                                  128 ** -0.5)
+    assert pkv.get_device_errors() & pkv.DEVERR_SEQLEN_RANGE
+    assert_attention_close(out[:100], ref[:100], "the sequence within the bound")
+    pkv.get_device_errors(reset=True)
+
+
 # ------------------------------------------------------------------ full-size workloads
 def _sampled_oracle(q_d, k_d, v_d, cq, ck, seqs, block_table=None, kc_d=None, vc_d=None):
     """Oracle on a few sequences, taking their rows back from the device."""
