@@ -49,6 +49,7 @@ typedef int32_t pkv_status;
 #define PKV_ERR_UNSUPPORTED 2 /* valid but not implemented: head_dim != 128, block_size % 256 */
 #define PKV_ERR_WORKSPACE 3   /* workspace missing or smaller than the query says */
 #define PKV_ERR_CUDA 4        /* a CUDA runtime/driver call failed (launch, tensor map) */
+#define PKV_ERR_NO_BLOCKS 5   /* block manager: not enough free blocks; nothing was changed */
 
 /* bits of the device-side error word */
 #define PKV_DEVERR_SLOT_RANGE 1u      /* kv_store: slot_mapping[t] >= num_slots */
@@ -247,6 +248,67 @@ pkv_status pkv_paged_decode_attn_noalloc(const void *q, const void *k_cache, con
                                          int32_t num_kv_heads, int32_t head_dim,
                                          int32_t block_size, int64_t num_blocks, float scale,
                                          int32_t num_splits, void *out, void *stream);
+
+/* ------------------------------------------------------------------ block manager (host)
+ *
+ * The owner of the pool's blocks on the host: «nano-vLLM 最小化vLLM重新实现», 架构 3 (块管理器)
+ * -- fixed-size blocks with a reference count and a hash, allocate() that reuses cached
+ * prefix blocks by hash and takes new blocks only for the rest, xxhash over token ids,
+ * preemption that frees a sequence's blocks; the per-sequence block list is the page table of
+ * «企业官网建设流程全解析 (Nano-vLLM 指南)» §2.2, the cached prefix of its §4.4. It produces
+ * the block tables that the attention calls read (slot of token i = table[i / block_size] *
+ * block_size + i % block_size). Host memory only, no CUDA; one handle must not be used by
+ * two threads at once. Rules:
+ *   - Only full blocks are hashed: XXH64 (seed 0) of the previous block's hash (8 bytes,
+ *     little-endian; absent for a sequence's first block) followed by the block's token ids
+ *     (int32, little-endian). A hit also needs equal token ids.
+ *   - Once a block of a sequence misses, the rest of the sequence gets new blocks.
+ *   - Free blocks are handed out first-in first-out, 0, 1, 2, ... at the start; a freed block
+ *     stays a possible hit until it is handed out again.
+ */
+typedef struct pkv_block_manager pkv_block_manager;
+
+/* A manager of num_blocks blocks of block_size tokens, all free. NULL on bad sizes or when
+ * out of host memory. Free it with pkv_bm_destroy. */
+pkv_block_manager *pkv_bm_create(int32_t num_blocks, int32_t block_size);
+void pkv_bm_destroy(pkv_block_manager *bm);
+
+/* Free blocks (-1 for a NULL handle); a block's reference count (-1 for a bad id); a block's
+ * hash, with *is_hashed = 0 for a block that is not full and registered. */
+int32_t pkv_bm_num_free(const pkv_block_manager *bm);
+int32_t pkv_bm_ref_count(const pkv_block_manager *bm, int32_t block);
+pkv_status pkv_bm_block_hash(const pkv_block_manager *bm, int32_t block, uint64_t *hash,
+                             int32_t *is_hashed);
+
+/* Blocks for a new (or preempted and resumed) sequence of num_tokens tokens: writes
+ * ceil(num_tokens / block_size) block ids to block_table (table_capacity entries available)
+ * and their count to *num_table_blocks, and the number of leading tokens whose K/V are
+ * already cached (a multiple of block_size) to *num_cached_tokens; a prefill then only has
+ * to compute the rest. PKV_ERR_NO_BLOCKS, with nothing changed, when fewer free blocks than
+ * ceil(num_tokens / block_size) are left. */
+pkv_status pkv_bm_allocate(pkv_block_manager *bm, const int32_t *token_ids, int32_t num_tokens,
+                           int32_t *block_table, int32_t table_capacity,
+                           int32_t *num_table_blocks, int32_t *num_cached_tokens);
+
+/* Release a finished or preempted sequence: each block's reference count drops by one (last
+ * block first); blocks that reach zero go to the back of the free list. PKV_ERR_INVALID_ARG,
+ * with nothing changed, for an id out of range or a block released more often than held. */
+pkv_status pkv_bm_deallocate(pkv_block_manager *bm, const int32_t *block_table,
+                             int32_t num_table_blocks);
+
+/* 1 if a sequence that now has seq_len tokens (its newest token included) can be given the
+ * block that token may need, else 0. */
+int32_t pkv_bm_can_append(const pkv_block_manager *bm, int32_t seq_len);
+
+/* After a token was appended (the sequence has seq_len tokens, token_ids holds all of them):
+ * takes a new block when the token starts one (appended to block_table, *num_table_blocks
+ * grows by one), and hashes and registers the last block when the token fills it. */
+pkv_status pkv_bm_may_append(pkv_block_manager *bm, const int32_t *token_ids, int32_t seq_len,
+                             int32_t *block_table, int32_t table_capacity,
+                             int32_t *num_table_blocks);
+
+/* XXH64 of len bytes (the hash the block manager uses), exported for tests. */
+uint64_t pkv_xxh64(const void *data, size_t len, uint64_t seed);
 
 #ifdef __cplusplus
 }

@@ -19,7 +19,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpkv.so")
 
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA = range(5)
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_NO_BLOCKS = range(6)
 DEVERR_SLOT_RANGE, DEVERR_BLOCK_RANGE, DEVERR_CONTEXT_RANGE = 1, 2, 4
 DEVERR_SEQLEN_RANGE, DEVERR_TIMEOUT = 8, 16
 
@@ -40,6 +40,18 @@ SIGNATURES = {
     "pkv_varlen_prefill_attn": (_I32, [_P, _I64, _I64, _P, _P, _I64, _I64, _P, _P, _I32, _I32,
                                        _I32, _P, _I32, _I32, _I64, _I32, _I32, _I32, _F, _I32,
                                        _P, _SZ, _P, _P]),
+    "pkv_bm_create": (_P, [_I32, _I32]),
+    "pkv_bm_destroy": (None, [_P]),
+    "pkv_bm_num_free": (_I32, [_P]),
+    "pkv_bm_ref_count": (_I32, [_P, _I32]),
+    "pkv_bm_block_hash": (_I32, [_P, _I32, ctypes.POINTER(ctypes.c_uint64),
+                                 ctypes.POINTER(ctypes.c_int32)]),
+    "pkv_bm_allocate": (_I32, [_P, _P, _I32, _P, _I32, ctypes.POINTER(ctypes.c_int32),
+                               ctypes.POINTER(ctypes.c_int32)]),
+    "pkv_bm_deallocate": (_I32, [_P, _P, _I32]),
+    "pkv_bm_can_append": (_I32, [_P, _I32]),
+    "pkv_bm_may_append": (_I32, [_P, _P, _I32, _P, _I32, ctypes.POINTER(ctypes.c_int32)]),
+    "pkv_xxh64": (ctypes.c_uint64, [_P, _SZ, ctypes.c_uint64]),
 }
 
 
@@ -226,3 +238,75 @@ def varlen_prefill_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
         int(max_seqlen_k), _ptr(block_table), W, bs, nb, hq, hkv, d, float(scale),
         int(bool(causal)), _ptr(workspace), workspace.numel(), _ptr(out), _stream(stream)))
     return out
+
+
+# ----------------------------------------------------------------------------- block manager
+def xxh64(data: bytes, seed: int = 0) -> int:
+    """XXH64 of a byte string, computed by the library (the block manager's hash)."""
+    buf = ctypes.create_string_buffer(bytes(data), max(1, len(data)))
+    return int(_LIB.pkv_xxh64(buf, len(data), seed))
+
+
+class BlockManager:
+    """Host-side block manager of libpkv (pkv_bm_* in include/pkv.h): blocks with reference
+    counts and prefix-cache hashes. Sequences are lists of int token ids; block tables are
+    lists of block ids. Every call goes to the C++ implementation."""
+
+    def __init__(self, num_blocks: int, block_size: int):
+        h = _LIB.pkv_bm_create(int(num_blocks), int(block_size))
+        if not h:
+            raise PkvError("pkv_bm_create", ERR_INVALID_ARG)
+        self._h = ctypes.c_void_p(h)
+        self.num_blocks, self.block_size = int(num_blocks), int(block_size)
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            _LIB.pkv_bm_destroy(h)
+            self._h = None
+
+    @staticmethod
+    def _ints(xs):
+        xs = list(xs)
+        return (ctypes.c_int32 * max(1, len(xs)))(*xs), len(xs)
+
+    @property
+    def num_free(self) -> int:
+        return int(_LIB.pkv_bm_num_free(self._h))
+
+    def ref_count(self, block: int) -> int:
+        return int(_LIB.pkv_bm_ref_count(self._h, int(block)))
+
+    def block_hash(self, block: int):
+        """The block's hash, or None while it is not full and registered."""
+        h, ok = ctypes.c_uint64(), ctypes.c_int32()
+        _check("pkv_bm_block_hash", _LIB.pkv_bm_block_hash(self._h, int(block),
+                                                             ctypes.byref(h), ctypes.byref(ok)))
+        return int(h.value) if ok.value else None
+
+    def allocate(self, token_ids):
+        """Block table and number of cached leading tokens for a new sequence."""
+        toks, n = self._ints(token_ids)
+        cap = max(1, -(-n // self.block_size))
+        table = (ctypes.c_int32 * cap)()
+        nb, cached = ctypes.c_int32(), ctypes.c_int32()
+        _check("pkv_bm_allocate", _LIB.pkv_bm_allocate(self._h, toks, n, table, cap,
+                                                       ctypes.byref(nb), ctypes.byref(cached)))
+        return list(table[:nb.value]), int(cached.value)
+
+    def deallocate(self, table) -> None:
+        t, n = self._ints(table)
+        _check("pkv_bm_deallocate", _LIB.pkv_bm_deallocate(self._h, t, n))
+
+    def can_append(self, seq_len: int) -> bool:
+        return bool(_LIB.pkv_bm_can_append(self._h, int(seq_len)))
+
+    def may_append(self, token_ids, table):
+        """After appending a token (token_ids = the whole sequence): the updated table."""
+        toks, n = self._ints(token_ids)
+        cap = len(table) + 1
+        t = (ctypes.c_int32 * cap)(*table)
+        nb = ctypes.c_int32(len(table))
+        _check("pkv_bm_may_append", _LIB.pkv_bm_may_append(self._h, toks, n, t, cap,
+                                                           ctypes.byref(nb)))
+        return list(t[:nb.value])

@@ -1,6 +1,6 @@
 """Build libpkv.so (the C-ABI CUDA library) in-tree with nvcc for sm_103a.
 
-Each .cu file is compiled in parallel to an object file, then linked into a shared library
+Each .cu file (and each host-only .cpp file) is compiled in parallel to an object file, then linked into a shared library
 next to this file. cudart is linked statically; the driver API is reached at run time
 through cudaGetDriverEntryPointByVersion, so no libcuda is needed at link time.
 """
@@ -55,7 +55,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if not force and not _stale():
         return LIB
     os.makedirs(OBJ_DIR, exist_ok=True)
-    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
     with cf.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
         objs = list(ex.map(lambda s: _compile(s, verbose), srcs))
     tmp = LIB + f".tmp{os.getpid()}"

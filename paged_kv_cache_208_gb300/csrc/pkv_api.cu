@@ -109,6 +109,7 @@ const char *pkv_status_string(pkv_status status) {
     case PKV_ERR_UNSUPPORTED: return "unsupported shape or layout";
     case PKV_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case PKV_ERR_CUDA: return "CUDA call failed";
+    case PKV_ERR_NO_BLOCKS: return "not enough free blocks";
     default: return "unknown status";
   }
 }
