@@ -350,6 +350,42 @@ def time_prefix_prefill(pkv, iters: int = 10):
             "l2": "the 8 shared prefix blocks (8 MiB of K+V) stay in L2 across sequences"}
 
 
+def time_qk_norm_rope_store(pkv, hbm_peak: float, iters: int = 20):
+    """QK RMSNorm + RoPE fused into the store, on the varlen prefill workload's new tokens
+    (145k tokens, positions within their prompts, the workload's slots)."""
+    lens = w.varlen_prefill_lengths()
+    lay = w.varlen_prefill_layout(num_blocks=w.blocks_needed(lens) + 64)
+    T = int(lens.sum())
+    g = w.rng(9)
+    qkv = w.device_bf16_normal((T, (HQ + 2 * HKV) * D), 901)
+    qw = torch.from_numpy(w.f32_to_bf16_bits(g.normal(1.0, 0.2, D).astype(np.float32))
+                          .view(np.int16)).view(torch.bfloat16).cuda()
+    kw = qw.clone()
+    table = torch.from_numpy(w.random_cos_sin_table(g, 1024, D)).cuda()
+    pos = torch.from_numpy(np.concatenate([np.arange(L) for L in lens]).astype(np.int64)).cuda()
+    slots = torch.from_numpy(lay.slot_mapping).cuda()
+    kc = torch.empty((lay.num_blocks, BS, HKV, D), dtype=torch.bfloat16, device="cuda")
+    vc = torch.empty_like(kc)
+    q = torch.empty((T, HQ, D), dtype=torch.bfloat16, device="cuda")
+    call = lambda: pkv.qk_norm_rope_store(qkv, pos, qw, kw, 1e-6, table, slots, kc, vc, HQ, HKV,
+                                          q_out=q)
+    for _ in range(3):
+        call()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(iters):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / 1e3 / iters
+    # projection rows in; q rows, K and V rows out; positions and slots
+    nbytes = T * ((HQ + 2 * HKV) * D * 2 + HQ * D * 2 + 2 * HKV * D * 2 + 16)
+    return {"tokens": T, "us": t * 1e6, "gbs": nbytes / t / 1e9, "bytes": nbytes,
+            "frac_of_hbm_peak": nbytes / t / 1e9 / hbm_peak,
+            "l2": "inputs (2.4 GB) larger than L2"}
+
+
 def time_prefill(pkv, iters: int = 10):
     """Varlen causal prefill attention: 256 prompts, lengths U[100, 1024], packed layout;
     one layer timed (x28 for a model)."""
@@ -482,6 +518,7 @@ def run_ours(args):
             {k: v for k, v in time_decode_shape(pkv, b, 1024, hbm_peak).items() if k in keep}
             for b in (1, 8, 64)]
         extra["kv_store_prefill"] = time_prefill_store(pkv)
+        extra["qk_norm_rope_store_prefill"] = time_qk_norm_rope_store(pkv, hbm_peak)
         extra["prefill"] = time_prefill(pkv)
         if "tflops" in extra["prefill"]:
             extra["prefill"]["frac_of_bf16_peak"] = extra["prefill"]["tflops"] / bf16_peak
@@ -610,6 +647,18 @@ def run_profile(args):
         vc = torch.empty_like(kc)
         slots = torch.from_numpy(lay.slot_mapping).cuda()
         run = lambda: pkv.kv_store(k, v, slots, kc, vc)
+    elif args.profile == "rope":
+        lens = w.varlen_prefill_lengths()
+        lay = w.varlen_prefill_layout(num_blocks=w.blocks_needed(lens) + 64)
+        T = int(lens.sum())
+        qkv = w.device_bf16_normal((T, (HQ + 2 * HKV) * D), 901)
+        qw = torch.ones(D, dtype=torch.bfloat16, device="cuda")
+        table = torch.from_numpy(w.random_cos_sin_table(w.rng(9), 1024, D)).cuda()
+        pos = torch.from_numpy(np.concatenate([np.arange(L) for L in lens]).astype(np.int64)).cuda()
+        slots = torch.from_numpy(lay.slot_mapping).cuda()
+        kc = torch.empty((lay.num_blocks, BS, HKV, D), dtype=torch.bfloat16, device="cuda")
+        vc = torch.empty_like(kc)
+        run = lambda: pkv.qk_norm_rope_store(qkv, pos, qw, qw, 1e-6, table, slots, kc, vc, HQ, HKV)
     elif args.profile == "prefix":
         lay = w.prefix_prefill_case_layout(num_blocks=8 + 64 * 3 + 32)
         kc = w.device_bf16_normal((lay.num_blocks, BS, HKV, D), 701)
@@ -654,7 +703,7 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--num-splits", type=int, default=0,
                     help="decode KV splits of the longest context (0 = the library's choice)")
-    ap.add_argument("--profile", choices=["decode", "prefill", "prefix", "store"],
+    ap.add_argument("--profile", choices=["decode", "prefill", "prefix", "store", "rope"],
                     help="run one kernel alone (for ncu); prints no benchmark line")
     args = ap.parse_args()
     if args.warmup < 3:

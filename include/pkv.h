@@ -57,6 +57,8 @@ typedef int32_t pkv_status;
 #define PKV_DEVERR_CONTEXT_RANGE 4u   /* decode: context_lens[b] < 0, > max_context_len,
                                          or > block_table_width * block_size */
 #define PKV_DEVERR_SEQLEN_RANGE 8u    /* prefill: bad cu_seqlens entry */
+#define PKV_DEVERR_POSITION_RANGE 32u /* qk_norm_rope_store: position outside the cos/sin
+                                         cache */
 #define PKV_DEVERR_TIMEOUT 16u        /* a pipeline wait gave up after 2 s. The bit is sticky:
                                          while it is set, every attention kernel of the library
                                          returns at once without computing, until
@@ -248,6 +250,38 @@ pkv_status pkv_paged_decode_attn_noalloc(const void *q, const void *k_cache, con
                                          int32_t num_kv_heads, int32_t head_dim,
                                          int32_t block_size, int64_t num_blocks, float scale,
                                          int32_t num_splits, void *out, void *stream);
+
+/*
+ * qk_norm_rope_store -- the step before the store, fused into it: «nano-vLLM 最小化vLLM重新实现»,
+ * 架构 6 模型 (the Qwen3 layer: RMSNorm of every query and key head -- QK 归一化 -- then RoPE;
+ * 辅助层: RotaryEmbedding reads a precomputed cos/sin cache), and 架构 5 (K/V written into
+ * the paged cache through slot_mapping).
+ *
+ * qkv:        [num_tokens, (Hq + 2 Hkv) * head_dim] bf16, token stride qkv_tok_stride
+ *             elements (a multiple of 8): Hq query heads, then Hkv key heads, then Hkv value
+ *             heads (the fused projection's output).
+ * positions:  [num_tokens] int64, the tokens' positions in their sequences.
+ * q_norm_weight, k_norm_weight: [head_dim] bf16.   eps: >= 0.
+ * cos_sin_cache: [max_position, head_dim] fp32; row p = cos of the half-dim angles of
+ *             position p, then their sines.
+ * For each query / key head x (fp32 arithmetic):
+ *     n = bf16_rne(x * rsqrt(mean(x^2) + eps) * w)
+ *     y_i = n_i c_i - n_{i+h} s_i,  y_{i+h} = n_{i+h} c_i + n_i s_i   (h = head_dim / 2,
+ *                                    c, s = row positions[t] of the cache; rotate-half RoPE)
+ * q_out [num_tokens, Hq, head_dim] bf16 (contiguous) gets the query heads' y (RNE); the key
+ * heads' y and the value heads (unchanged) go to k_cache / v_cache row slot_mapping[t] exactly
+ * as pkv_kv_store writes them (negative slot: nothing stored, q still written; slot >=
+ * num_slots: skipped and PKV_DEVERR_SLOT_RANGE). A position outside [0, max_position) skips the
+ * token's query and key heads and sets PKV_DEVERR_POSITION_RANGE.
+ * Implemented: head_dim == 128, 16-byte aligned pointers. Asynchronous on `stream`.
+ */
+pkv_status pkv_qk_norm_rope_store(const void *qkv, int64_t qkv_tok_stride, int64_t num_tokens,
+                                  const int64_t *positions, const void *q_norm_weight,
+                                  const void *k_norm_weight, float eps,
+                                  const float *cos_sin_cache, int64_t max_position,
+                                  const int64_t *slot_mapping, void *q_out, void *k_cache,
+                                  void *v_cache, int64_t num_slots, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t head_dim, void *stream);
 
 /* ------------------------------------------------------------------ block manager (host)
  *

@@ -16,10 +16,10 @@ import numpy as np
 
 from . import build as _build
 
-OK, BAD_SLOT, DUP_SLOT, BAD_BLOCK, BAD_ARG, NO_MEMORY = range(6)
+OK, BAD_SLOT, DUP_SLOT, BAD_BLOCK, BAD_ARG, NO_MEMORY, BAD_POSITION = range(7)
 _ERRORS = {BAD_SLOT: "slot out of range", DUP_SLOT: "duplicate slot in one call",
            BAD_BLOCK: "block id out of range / table too narrow", BAD_ARG: "bad argument",
-           NO_MEMORY: "out of host memory"}
+           NO_MEMORY: "out of host memory", BAD_POSITION: "position outside the cos/sin cache"}
 
 
 class OracleError(RuntimeError):
@@ -47,6 +47,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.pkv_oracle_varlen_prefill.restype = _I32
     lib.pkv_oracle_varlen_prefill.argtypes = [_P, _I64, _P, _P, _I64, _P, _P, _I32, _P, _I32,
                                               _I32, _I64, _I32, _I32, _I32, _D, _I32, _P, _I32]
+    lib.pkv_oracle_qk_norm_rope.restype = _I32
+    lib.pkv_oracle_qk_norm_rope.argtypes = [_P, _I64, _I64, _P, _P, _P, _D, _P, _I64, _I32,
+                                            _I32, _I32, _P, _P, _P, _P]
     return lib
 
 
@@ -141,3 +144,28 @@ def varlen_prefill(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, *, causal:
     if rc:
         raise OracleError(rc)
     return out
+
+
+def qk_norm_rope(qkv, positions, q_weight, k_weight, eps: float, cos_sin, num_q_heads: int,
+                 num_kv_heads: int, *, L: ctypes.CDLL | None = None):
+    """qkv [T, (Hq + 2 Hkv) * D] (or a strided view with dense rows) uint16 bf16 bits;
+    positions [T]; weights [D] uint16; cos_sin [max_position, D] float32.
+    Returns (q [T, Hq, D], k [T, Hkv, D], q_normed, k_normed), float64."""
+    L = L or lib()
+    qkv = np.asarray(qkv, np.uint16)
+    T = qkv.shape[0]
+    D = int(np.asarray(q_weight).shape[0])
+    assert qkv.strides[-1] == 2
+    ts = qkv.strides[0] // 2 if T else (num_q_heads + 2 * num_kv_heads) * D
+    pos = _c(positions, np.int64)
+    qw, kw = _c(q_weight, np.uint16), _c(k_weight, np.uint16)
+    cs = _c(cos_sin, np.float32)
+    q = np.zeros((T, num_q_heads, D)); k = np.zeros((T, num_kv_heads, D))
+    qn = np.zeros_like(q); kn = np.zeros_like(k)
+    rc = L.pkv_oracle_qk_norm_rope(qkv.ctypes.data_as(_P), ts, T, _ptr(pos), _ptr(qw), _ptr(kw),
+                                   float(eps), _ptr(cs), cs.shape[0], num_q_heads, num_kv_heads,
+                                   D, _ptr(q), _ptr(k), _ptr(qn), _ptr(kn))
+    if rc:
+        raise OracleError(rc)
+    return q, k, qn, kn
+

@@ -42,7 +42,7 @@
 #endif
 
 enum { ORACLE_OK = 0, ORACLE_BAD_SLOT = 1, ORACLE_DUP_SLOT = 2, ORACLE_BAD_BLOCK = 3,
-       ORACLE_BAD_ARG = 4, ORACLE_NO_MEMORY = 5 };
+       ORACLE_BAD_ARG = 4, ORACLE_NO_MEMORY = 5, ORACLE_BAD_POSITION = 6 };
 
 /* bf16 is the top half of an IEEE binary32; widening to double is exact. */
 static double bf16_value(uint16_t bits)
@@ -252,4 +252,60 @@ int32_t pkv_oracle_varlen_prefill(const uint16_t *q, int64_t q_tok_stride, const
         }
     }
     return status;
+}
+
+/*
+ * QK normalisation and rotary position embedding of one layer's new tokens -- the step just
+ * before the store. [nano-vLLM 最小化vLLM重新实现] 架构 6 模型: the Qwen3 layer applies an
+ * RMSNorm to every query and key head (QK 归一化) and RoPE; 辅助层: RotaryEmbedding reads a
+ * precomputed cos/sin cache.
+ *
+ * Token t's fused projection row (token stride tok_stride elements) holds num_q_heads query
+ * heads, then num_kv_heads key heads, then num_kv_heads value heads, head_dim values each.
+ * For a query or key head x with weight w (q_weight or k_weight, head_dim values):
+ *     n_d = x_d / sqrt(mean_e(x_e^2) + eps) * w_d                              (RMSNorm)
+ *     with half = head_dim / 2, c_i = cos_sin[pos, i], s_i = cos_sin[pos, half + i]:
+ *     y_i        = n_i c_i - n_{i+half} s_i,   y_{i+half} = n_{i+half} c_i + n_i s_i
+ * (the rotate-half pairing of element i with i + half). q_out [T, Hq, D] and k_out
+ * [T, Hkv, D] get y; q_normed / k_normed get n (the test's error bound uses them). Value
+ * heads pass through unchanged (the store copies them). A position outside
+ * [0, max_position) is an error.
+ */
+int32_t pkv_oracle_qk_norm_rope(const uint16_t *qkv, int64_t tok_stride, int64_t num_tokens,
+                                const int64_t *positions, const uint16_t *q_weight,
+                                const uint16_t *k_weight, double eps, const float *cos_sin,
+                                int64_t max_position, int32_t num_q_heads, int32_t num_kv_heads,
+                                int32_t head_dim, double *q_out, double *k_out,
+                                double *q_normed, double *k_normed)
+{
+    if (num_tokens < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        head_dim % 2 != 0 || tok_stride < (int64_t)(num_q_heads + 2 * num_kv_heads) * head_dim)
+        return ORACLE_BAD_ARG;
+    for (int64_t t = 0; t < num_tokens; ++t)
+        if (positions[t] < 0 || positions[t] >= max_position) return ORACLE_BAD_POSITION;
+    const int32_t half = head_dim / 2;
+    const int32_t heads = num_q_heads + num_kv_heads;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        const float *cs = cos_sin + positions[t] * head_dim;
+        for (int32_t h = 0; h < heads; ++h) {
+            const int is_q = h < num_q_heads;
+            const uint16_t *x = qkv + t * tok_stride + (int64_t)h * head_dim;
+            const uint16_t *w = is_q ? q_weight : k_weight;
+            const int64_t orow = is_q ? (t * num_q_heads + h) * head_dim
+                                      : (t * num_kv_heads + (h - num_q_heads)) * head_dim;
+            double *n = (is_q ? q_normed : k_normed) + orow;
+            double *y = (is_q ? q_out : k_out) + orow;
+            double ss = 0.0;
+            for (int32_t d = 0; d < head_dim; ++d) ss += bf16_value(x[d]) * bf16_value(x[d]);
+            const double r = 1.0 / sqrt(ss / head_dim + eps);
+            for (int32_t d = 0; d < head_dim; ++d) n[d] = bf16_value(x[d]) * r * bf16_value(w[d]);
+            for (int32_t i = 0; i < half; ++i) {
+                const double c = cs[i], sn = cs[half + i];
+                y[i] = n[i] * c - n[i + half] * sn;
+                y[i + half] = n[i + half] * c + n[i] * sn;
+            }
+        }
+    }
+    return ORACLE_OK;
 }

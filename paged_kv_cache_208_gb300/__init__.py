@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_HERE, "libpkv.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_NO_BLOCKS = range(6)
 DEVERR_SLOT_RANGE, DEVERR_BLOCK_RANGE, DEVERR_CONTEXT_RANGE = 1, 2, 4
-DEVERR_SEQLEN_RANGE, DEVERR_TIMEOUT = 8, 16
+DEVERR_SEQLEN_RANGE, DEVERR_TIMEOUT, DEVERR_POSITION_RANGE = 8, 16, 32
 
 # symbol -> (restype, argtypes); mirrors include/pkv.h
 _P, _I32, _I64, _F, _SZ = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
@@ -40,6 +40,8 @@ SIGNATURES = {
     "pkv_varlen_prefill_attn": (_I32, [_P, _I64, _I64, _P, _P, _I64, _I64, _P, _P, _I32, _I32,
                                        _I32, _P, _I32, _I32, _I64, _I32, _I32, _I32, _F, _I32,
                                        _P, _SZ, _P, _P]),
+    "pkv_qk_norm_rope_store": (_I32, [_P, _I64, _I64, _P, _P, _P, _F, _P, _I64, _P, _P, _P,
+                                      _P, _I64, _I32, _I32, _I32, _P]),
     "pkv_bm_create": (_P, [_I32, _I32]),
     "pkv_bm_destroy": (None, [_P]),
     "pkv_bm_num_free": (_I32, [_P]),
@@ -238,6 +240,34 @@ def varlen_prefill_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
         int(max_seqlen_k), _ptr(block_table), W, bs, nb, hq, hkv, d, float(scale),
         int(bool(causal)), _ptr(workspace), workspace.numel(), _ptr(out), _stream(stream)))
     return out
+
+
+def qk_norm_rope_store(qkv, positions, q_norm_weight, k_norm_weight, eps, cos_sin_cache,
+                       slot_mapping, k_cache, v_cache, num_q_heads: int, num_kv_heads: int,
+                       q_out=None, stream=None):
+    """QK RMSNorm + RoPE of the new tokens, K/V stored into the pool, q returned.
+
+    qkv: [T, (Hq + 2 Hkv) * D] bf16 (rows may be a strided view); positions, slot_mapping:
+    [T] int64; weights [D] bf16; cos_sin_cache [max_position, D] float32; pools
+    [NB, bs, Hkv, D] bf16. Returns q [T, Hq, D] bf16."""
+    T = qkv.shape[0]
+    D = q_norm_weight.shape[0]
+    assert qkv.dtype == torch.bfloat16 and qkv.is_cuda and qkv.stride(-1) == 1
+    for t in (q_norm_weight, k_norm_weight, k_cache, v_cache):
+        assert t.dtype == torch.bfloat16 and t.is_cuda and t.is_contiguous()
+    assert cos_sin_cache.dtype == torch.float32 and cos_sin_cache.is_contiguous()
+    assert positions.dtype == torch.int64 and slot_mapping.dtype == torch.int64
+    positions, slot_mapping = positions.contiguous(), slot_mapping.contiguous()
+    if q_out is None:
+        q_out = torch.empty((T, num_q_heads, D), dtype=torch.bfloat16, device=qkv.device)
+    num_slots = k_cache.numel() // (num_kv_heads * D)
+    _check("pkv_qk_norm_rope_store", _LIB.pkv_qk_norm_rope_store(
+        qkv.data_ptr(), qkv.stride(0) if T else qkv.shape[-1], T, positions.data_ptr(),
+        q_norm_weight.data_ptr(), k_norm_weight.data_ptr(), float(eps),
+        cos_sin_cache.data_ptr(), cos_sin_cache.shape[0], slot_mapping.data_ptr(),
+        q_out.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), num_slots, num_q_heads,
+        num_kv_heads, D, _stream(stream)))
+    return q_out
 
 
 # ----------------------------------------------------------------------------- block manager

@@ -297,6 +297,121 @@ def pin_prefill_rows_without_keys_are_zero(L):
     np.testing.assert_allclose(out[3:], want.transpose(1, 0, 2), rtol=1e-12, atol=1e-12)
 
 
+# ------------------------------------------------------------- QK normalisation + RoPE
+def _qkv_case(T, hq, hkv, d, seed):
+    g = w.rng(seed)
+    return w.host_bf16_normal(g, (T, (hq + 2 * hkv) * d)), g
+
+
+def _table(angles: np.ndarray) -> np.ndarray:
+    """cos/sin table rows [cos(a_0..a_{h-1}), sin(a_0..a_{h-1})] as float32."""
+    return np.concatenate([np.cos(angles), np.sin(angles)], axis=-1).astype(np.float32)
+
+
+ONE = 0x3F80  # bf16 1.0
+
+
+def pin_qknorm_unit_rms_and_direction(L):
+    """Weight 1, eps 0, no rotation: every head comes out with RMS exactly 1, in the direction
+    of its input."""
+    d, hq, hkv = 16, 3, 2
+    qkv, _ = _qkv_case(5, hq, hkv, d, 1)
+    one = np.full(d, ONE, np.uint16)
+    q, k, qn, kn = oracle.qk_norm_rope(qkv, np.zeros(5), one, one, 0.0, _table(np.zeros((1, d // 2))),
+                                       hq, hkv, L=L)
+    np.testing.assert_allclose(q, qn, rtol=0, atol=0)
+    x = _f64(qkv).reshape(5, hq + 2 * hkv, d)
+    for y, xs in ((qn, x[:, :hq]), (kn, x[:, hq:hq + hkv])):
+        np.testing.assert_allclose(np.sqrt((y ** 2).mean(-1)), 1.0, rtol=1e-12)
+        cosang = (y * xs).sum(-1) / np.linalg.norm(y, axis=-1) / np.linalg.norm(xs, axis=-1)
+        np.testing.assert_allclose(cosang, 1.0, rtol=1e-12)
+
+
+def pin_qknorm_eps_closed_form(L):
+    """A constant head of value c with eps: each element becomes c / sqrt(c^2 + eps)."""
+    d = 8
+    qkv = np.full((1, 3 * d), ONE, np.uint16)                    # all ones, hq = hkv = 1
+    one = np.full(d, ONE, np.uint16)
+    _, _, qn, kn = oracle.qk_norm_rope(qkv, [0], one, one, 0.5, _table(np.zeros((1, d // 2))),
+                                       1, 1, L=L)
+    np.testing.assert_allclose(qn, 1 / np.sqrt(1.5), rtol=1e-14)
+    np.testing.assert_allclose(kn, 1 / np.sqrt(1.5), rtol=1e-14)
+
+
+def pin_qknorm_weight_is_elementwise(L):
+    d, hq, hkv = 16, 2, 1
+    qkv, g = _qkv_case(3, hq, hkv, d, 2)
+    one = np.full(d, ONE, np.uint16)
+    wq, wk = w.host_bf16_normal(g, (d,)), w.host_bf16_normal(g, (d,))
+    t = _table(np.zeros((1, d // 2)))
+    _, _, qn1, kn1 = oracle.qk_norm_rope(qkv, np.zeros(3), one, one, 1e-6, t, hq, hkv, L=L)
+    _, _, qn, kn = oracle.qk_norm_rope(qkv, np.zeros(3), wq, wk, 1e-6, t, hq, hkv, L=L)
+    np.testing.assert_allclose(qn, qn1 * _f64(wq), rtol=1e-14)
+    np.testing.assert_allclose(kn, kn1 * _f64(wk), rtol=1e-14)
+
+
+def pin_rope_rotates_i_with_i_plus_half(L):
+    """A head that is the unit vector e_i (normalised to sqrt(d) e_i) at angle a_i: element i
+    becomes sqrt(d) cos a_i and element i + d/2 becomes sqrt(d) sin a_i (and e_{i+d/2} gives
+    -sqrt(d) sin a_i and sqrt(d) cos a_i); nothing else changes."""
+    d, half = 8, 4
+    angles = np.array([[0.3, -1.1, 2.0, 0.7]])
+    one = np.full(d, ONE, np.uint16)
+    for i in range(d):
+        qkv = np.zeros((1, 3 * d), np.uint16)
+        qkv[0, i] = ONE
+        qkv[0, d + i] = ONE
+        q, k, _, _ = oracle.qk_norm_rope(qkv, [0], one, one, 0.0, _table(angles), 1, 1, L=L)
+        t = _table(angles).astype(np.float64)[0]
+        c, s = t[i % half], t[half + i % half]
+        want = np.zeros(d)
+        if i < half:
+            want[i], want[i + half] = c, s
+        else:
+            want[i - half], want[i] = -s, c
+        want *= np.sqrt(d)
+        np.testing.assert_allclose(q[0, 0], want, atol=1e-12)
+        np.testing.assert_allclose(k[0, 0], want, atol=1e-12)
+
+
+def pin_rope_relative_position(L):
+    """With the standard table (angle p * 10000^(-2i/d)), the score between a rotated query at
+    position m and key at n depends on m - n only."""
+    d, hq, hkv = 32, 1, 1
+    P = 64
+    inv = 10000.0 ** (-np.arange(0, d, 2) / d)
+    table = _table(np.arange(P)[:, None] * inv[None, :])
+    qkv, _ = _qkv_case(1, hq, hkv, d, 3)
+    one = np.full(d, ONE, np.uint16)
+    rows = np.repeat(qkv, 4, axis=0)
+    q, k, _, _ = oracle.qk_norm_rope(rows, [5, 20, 2, 17], one, one, 1e-6, table, hq, hkv, L=L)
+    # (m, n) = (5, 2) and (20, 17): the same distance
+    np.testing.assert_allclose((q[0, 0] * k[2, 0]).sum(), (q[1, 0] * k[3, 0]).sum(), rtol=1e-5)
+
+
+def pin_rope_keeps_pair_norms(L):
+    d, hq, hkv = 16, 2, 2
+    qkv, g = _qkv_case(4, hq, hkv, d, 4)
+    one = np.full(d, ONE, np.uint16)
+    table = _table(g.uniform(-np.pi, np.pi, (7, d // 2)))
+    q, k, qn, kn = oracle.qk_norm_rope(qkv, [0, 6, 3, 3], one, one, 1e-6, table, hq, hkv, L=L)
+    for y, n in ((q, qn), (k, kn)):
+        h = d // 2
+        np.testing.assert_allclose(y[..., :h] ** 2 + y[..., h:] ** 2,
+                                   n[..., :h] ** 2 + n[..., h:] ** 2, rtol=1e-6)
+
+
+def pin_qknorm_rejects_bad_position(L):
+    qkv, _ = _qkv_case(2, 1, 1, 8, 5)
+    one = np.full(8, ONE, np.uint16)
+    try:
+        oracle.qk_norm_rope(qkv, [0, 4], one, one, 0.0, _table(np.zeros((4, 4))), 1, 1, L=L)
+    except oracle.OracleError as e:
+        assert e.code == oracle.BAD_POSITION
+    else:
+        raise AssertionError("position 4 of a 4-row table was accepted")
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
 
 

@@ -47,6 +47,16 @@ MUTANTS = [
      "k_cache[slot * row + e] = k[t * row + e];", None),
     ("store_skips_duplicate_check", "if (seen[slot]) { free(seen); return ORACLE_DUP_SLOT; }",
      "", None),
+    ("rms_sum_not_mean", "1.0 / sqrt(ss / head_dim + eps)", "1.0 / sqrt(ss + eps)", None),
+    ("rms_eps_dropped", "1.0 / sqrt(ss / head_dim + eps)", "1.0 / sqrt(ss / head_dim)", None),
+    ("norm_weight_dropped", "n[d] = bf16_value(x[d]) * r * bf16_value(w[d]);",
+     "n[d] = bf16_value(x[d]) * r;", None),
+    ("rope_sin_sign_flipped", "y[i + half] = n[i + half] * c + n[i] * sn;",
+     "y[i + half] = n[i + half] * c - n[i] * sn;", None),
+    ("rope_cos_sin_swapped", "const double c = cs[i], sn = cs[half + i];",
+     "const double c = cs[half + i], sn = cs[i];", None),
+    ("rope_pairs_adjacent", "y[i] = n[i] * c - n[i + half] * sn;",
+     "y[i] = n[i] * c - n[i ^ 1] * sn;", None),
 ]
 
 

@@ -407,3 +407,11 @@ def suffix_rows(lay: PrefillLayout) -> np.ndarray:
     cu_k = lay.cu_seqlens_k
     return np.concatenate([cu_k[n] + lay.prefix_len + np.arange(int(lay.seqlens_q[n]))
                            for n in range(lay.n)] + [np.zeros(0, np.int64)]).astype(np.int64)
+
+
+def random_cos_sin_table(g: np.random.Generator, max_position: int, head_dim: int) -> np.ndarray:
+    """[max_position, head_dim] float32: cosines of seeded random angles in [-pi, pi), then
+    their sines -- an arbitrary rotation table of the layout the RoPE step reads (the
+    kernels and the oracle take any table; none of the method is in how it is drawn)."""
+    a = g.uniform(-np.pi, np.pi, (max_position, head_dim // 2))
+    return np.concatenate([np.cos(a), np.sin(a)], axis=1).astype(np.float32)
