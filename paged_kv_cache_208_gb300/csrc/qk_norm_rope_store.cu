@@ -15,12 +15,15 @@
 // with c = cos_sin[pos, 0:64], s = cos_sin[pos, 64:128], rounded to bf16 (RNE): query heads
 // to q_out, key heads to k_cache[slot]; value heads are copied to v_cache[slot] bit for bit.
 //
-// A quarter warp (8 lanes) owns one head row: lane l holds elements 8l..8l+7 and their RoPE
+// A quarter warp (8 lanes) owns a head row: lane l holds elements 8l..8l+7 and their RoPE
 // partners 64+8l..64+8l+7 (16-byte loads and stores), so the rotation needs no exchange and
-// the sum of squares takes three shuffles. A warp does four rows; HBM traffic per token is
-// its projection row in and q, K and V out.
+// the sum of squares takes three shuffles. A warp does eight rows, two per quarter; HBM
+// traffic per token is its projection row in and q, K and V out. Roundings to bf16 go two
+// values per conversion instruction.
 #include <math.h>
 #include <stdint.h>
+
+#include <cuda_bf16.h>
 
 #include "device_common.cuh"
 #include "launch.h"
@@ -32,7 +35,8 @@ namespace {
 constexpr int kD = 128;
 constexpr int kHalf = kD / 2;
 constexpr int kThreads = 256;
-constexpr int kRowsPerWarp = 4;
+constexpr int kRowsPerWarp = 4;     // quarter warps
+constexpr int kRowsPerQuarter = 2;  // head rows each quarter warp processes
 
 struct RopeParams {
   const uint16_t *qkv;
@@ -59,67 +63,84 @@ __device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     f[2 * i] = bf(w[i] & 0xFFFFu);
-    f[2 * i + 1] = bf(w[i] >> 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
   }
 }
+// two floats to a bf16 pair (RNE), one conversion instruction
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&v);
+}
 __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
-  uint32_t w[4];
+  return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
+}
+// round to bf16 and back (the normalised activation is bf16, as between the model's layers)
+__device__ __forceinline__ void round8(float (&f)[8]) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
-    w[i] = (uint32_t)bf16_bits_rn(f[2 * i]) | ((uint32_t)bf16_bits_rn(f[2 * i + 1]) << 16);
-  return make_uint4(w[0], w[1], w[2], w[3]);
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t w = pack2(f[2 * i], f[2 * i + 1]);
+    f[2 * i] = bf(w & 0xFFFFu);
+    f[2 * i + 1] = __uint_as_float(w & 0xFFFF0000u);
+  }
 }
 
-__global__ void __launch_bounds__(kThreads) qk_norm_rope_store_kernel(const RopeParams p) {
-  const int lane = threadIdx.x & 31;
-  const int group = lane >> 3, gl = lane & 7;
-  const int heads = p.hq + 2 * p.hkv;
-  const int64_t row = ((int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) *
-                          kRowsPerWarp + group;
-  const bool live = row < p.num_tokens * heads;
-  const int64_t t = live ? row / heads : 0;
-  const int h = live ? (int)(row % heads) : 0;
-  const uint16_t *src = p.qkv + t * p.tok_stride + (int64_t)h * kD;
-  const uint4 *lo_src = reinterpret_cast<const uint4 *>(src + 8 * gl);
-  const uint4 *hi_src = reinterpret_cast<const uint4 *>(src + kHalf + 8 * gl);
-  const int64_t slot = live && h >= p.hq ? p.slots[t] : -1;
-  const bool slot_ok = slot >= 0 && slot < p.num_slots;
-  if (live && h >= p.hq && slot >= p.num_slots && gl == 0) record_error(p.err, 1u /* SLOT */);
+struct Row {
+  bool live;
+  int64_t t;
+  int h;
+  uint4 lo, hi;
+  float ss;
+};
 
-  // every lane loads and joins the shuffles before any lane leaves (full-warp shuffles)
-  const uint4 lo = live ? ld_stream_u4(lo_src) : make_uint4(0, 0, 0, 0);
-  const uint4 hi = live ? ld_stream_u4(hi_src) : make_uint4(0, 0, 0, 0);
-  float a[8], b[8];
-  unpack8(lo, a);
-  unpack8(hi, b);
-  float ss = 0.f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) ss = fmaf(a[i], a[i], fmaf(b[i], b[i], ss));
-  // the quarter warp's sum (lanes 8g..8g+7)
-  ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-  ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-  ss += __shfl_xor_sync(0xffffffffu, ss, 4);
-  if (!live) return;
-  if (h >= p.hq + p.hkv) {  // value head: straight copy
+__device__ __forceinline__ Row load_row(const RopeParams &p, int64_t row, int heads, int gl) {
+  Row r;
+  r.live = row < p.num_tokens * heads;
+  r.t = r.live ? row / heads : 0;
+  r.h = r.live ? (int)(row % heads) : 0;
+  const uint16_t *src = p.qkv + r.t * p.tok_stride + (int64_t)r.h * kD;
+  r.lo = r.live ? ld_stream_u4(reinterpret_cast<const uint4 *>(src + 8 * gl))
+                : make_uint4(0, 0, 0, 0);
+  r.hi = r.live ? ld_stream_u4(reinterpret_cast<const uint4 *>(src + kHalf + 8 * gl))
+                : make_uint4(0, 0, 0, 0);
+  return r;
+}
+
+// One head row after its sum of squares is known (no shuffles from here on).
+__device__ __forceinline__ void finish_row(const RopeParams &p, const Row &r, int gl) {
+  if (!r.live) return;
+  const bool is_v = r.h >= p.hq + p.hkv, is_q = r.h < p.hq;
+  const int64_t slot = is_q ? -1 : p.slots[r.t];
+  const bool slot_ok = slot >= 0 && slot < p.num_slots;
+  if (!is_q && slot >= p.num_slots && gl == 0) record_error(p.err, 1u /* SLOT_RANGE */);
+  if (is_v) {  // value head: straight copy
     if (slot_ok) {
-      uint16_t *dst = p.v_cache + slot * ((int64_t)p.hkv * kD) + (int64_t)(h - p.hq - p.hkv) * kD;
-      reinterpret_cast<uint4 *>(dst + 8 * gl)[0] = lo;
-      reinterpret_cast<uint4 *>(dst + kHalf + 8 * gl)[0] = hi;
+      uint16_t *dst =
+          p.v_cache + slot * ((int64_t)p.hkv * kD) + (int64_t)(r.h - p.hq - p.hkv) * kD;
+      reinterpret_cast<uint4 *>(dst + 8 * gl)[0] = r.lo;
+      reinterpret_cast<uint4 *>(dst + kHalf + 8 * gl)[0] = r.hi;
     }
     return;
   }
-  const int64_t pos = p.positions[t];
+  const int64_t pos = p.positions[r.t];
   if (pos < 0 || pos >= p.max_position) {
     if (gl == 0) record_error(p.err, 32u /* POSITION_RANGE */);
     return;
   }
-  const bool is_q = h < p.hq;
   if (!is_q && !slot_ok) return;
-  const float r = rsqrtf(ss * (1.f / kD) + p.eps);
+  const float rs = rsqrtf(r.ss * (1.f / kD) + p.eps);
   const uint16_t *wsrc = is_q ? p.q_weight : p.k_weight;
-  float wa[8], wb[8];
+  float a[8], b[8], wa[8], wb[8];
+  unpack8(r.lo, a);
+  unpack8(r.hi, b);
   unpack8(*reinterpret_cast<const uint4 *>(wsrc + 8 * gl), wa);
   unpack8(*reinterpret_cast<const uint4 *>(wsrc + kHalf + 8 * gl), wb);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    a[i] = a[i] * rs * wa[i];
+    b[i] = b[i] * rs * wb[i];
+  }
+  round8(a);
+  round8(b);
   const float4 *cs = reinterpret_cast<const float4 *>(p.cos_sin + pos * kD);
   const float4 c0 = cs[2 * gl], c1 = cs[2 * gl + 1];
   const float4 s0 = cs[16 + 2 * gl], s1 = cs[16 + 2 * gl + 1];
@@ -128,16 +149,45 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_store_kernel(const Rope
   float ya[8], yb[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    // the normalised activation is bf16, as between the model's layers
-    const float na = bf(bf16_bits_rn(a[i] * r * wa[i]));
-    const float nb = bf(bf16_bits_rn(b[i] * r * wb[i]));
-    ya[i] = na * c[i] - nb * s[i];
-    yb[i] = nb * c[i] + na * s[i];
+    ya[i] = a[i] * c[i] - b[i] * s[i];
+    yb[i] = b[i] * c[i] + a[i] * s[i];
   }
-  uint16_t *dst = is_q ? p.q_out + (t * p.hq + h) * kD
-                       : p.k_cache + slot * ((int64_t)p.hkv * kD) + (int64_t)(h - p.hq) * kD;
+  uint16_t *dst = is_q ? p.q_out + (r.t * p.hq + r.h) * kD
+                       : p.k_cache + slot * ((int64_t)p.hkv * kD) + (int64_t)(r.h - p.hq) * kD;
   reinterpret_cast<uint4 *>(dst + 8 * gl)[0] = pack8(ya);
   reinterpret_cast<uint4 *>(dst + kHalf + 8 * gl)[0] = pack8(yb);
+}
+
+__device__ __forceinline__ float sum_sq(const uint4 lo, const uint4 hi) {
+  float a[8], b[8];
+  unpack8(lo, a);
+  unpack8(hi, b);
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) ss = fmaf(a[i], a[i], fmaf(b[i], b[i], ss));
+  return ss;
+}
+
+// A quarter warp owns two head rows (base + g and base + 4 + g of the warp's eight): all
+// four 16-byte loads are issued before any arithmetic, so each lane keeps 64 bytes in flight.
+__global__ void __launch_bounds__(kThreads) qk_norm_rope_store_kernel(const RopeParams p) {
+  const int lane = threadIdx.x & 31;
+  const int group = lane >> 3, gl = lane & 7;
+  const int heads = p.hq + 2 * p.hkv;
+  const int64_t base = ((int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) *
+                       (kRowsPerQuarter * kRowsPerWarp);
+  Row r0 = load_row(p, base + group, heads, gl);
+  Row r1 = load_row(p, base + kRowsPerWarp + group, heads, gl);
+  r0.ss = sum_sq(r0.lo, r0.hi);
+  r1.ss = sum_sq(r1.lo, r1.hi);
+  // each quarter warp's sums (lanes 8g..8g+7); every lane of the warp takes part
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) {
+    r0.ss += __shfl_xor_sync(0xffffffffu, r0.ss, o);
+    r1.ss += __shfl_xor_sync(0xffffffffu, r1.ss, o);
+  }
+  finish_row(p, r0, gl);
+  finish_row(p, r1, gl);
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -169,7 +219,7 @@ extern "C" pkv_status pkv_qk_norm_rope_store(
   unsigned int *err = current_error_word();
   if (!err) return PKV_ERR_CUDA;
   const int64_t rows = num_tokens * (num_q_heads + 2 * num_kv_heads);
-  const int64_t rows_per_cta = (kThreads / 32) * kRowsPerWarp;
+  const int64_t rows_per_cta = (kThreads / 32) * kRowsPerQuarter * kRowsPerWarp;
   const int64_t grid = (rows + rows_per_cta - 1) / rows_per_cta;
   if (grid > INT32_MAX) return PKV_ERR_UNSUPPORTED;
   RopeParams prm{};
