@@ -494,13 +494,17 @@ DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
     p.chunk = (int32_t)((per + kTile - 1) / kTile * kTile);
   } else {
     // Each unit ends with a merge across the CTA's warps, so long units (up to 16 tiles) pay
-    // off; the work queue balances them as long as there are >= 4 units per CTA slot (two
-    // per SM). Take the longest chunk that keeps that many units.
+    // off, but one CTA streams a unit through a 3-tile ring, which caps its own bandwidth:
+    // enough units must run at once to fill HBM. Measured over batches 1..256 of 1024- and
+    // 2048-token contexts, the best choice is the longest chunk that still leaves about
+    // 1.5 units per SM (the work queue balances the rest).
+    // The split count is chosen first and the context divided evenly among the splits.
     const int64_t units = (int64_t)batch * num_kv_heads * p.head_groups;
-    const int64_t target = (int64_t)num_sms * 2 * 4;
-    int64_t chunk = 16 * kTile;
-    while (chunk > kTile && units * ((max_ctx + chunk - 1) / chunk) < target) chunk -= kTile;
-    p.chunk = (int32_t)chunk;
+    const int64_t target = (int64_t)num_sms * 3 / 2;
+    int64_t S = (max_tiles + 15) / 16;  // at most 16 tiles per unit
+    while (S < max_tiles && units * S < target) ++S;
+    const int64_t per = (max_ctx + S - 1) / S;
+    p.chunk = (int32_t)((per + kTile - 1) / kTile * kTile);
   }
   p.splits = (int32_t)((max_ctx + p.chunk - 1) / p.chunk);
   const size_t partials =
