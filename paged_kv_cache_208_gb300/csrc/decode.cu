@@ -11,7 +11,8 @@
 //
 // Persistent kernel: two CTAs per SM take units from a global queue (one atomic counter in
 // the workspace; units ordered split-major with the KV heads of a sequence adjacent, so the
-// CTAs reading one sequence's rows run together). Per CTA, 8 consumer warps + 1 producer
+// CTAs reading one sequence's rows run together). When there are no more units than CTAs,
+// CTA i takes unit i and the counter is not used. Per CTA, 8 consumer warps + 1 producer
 // warp:
 //   producer  -- takes a unit, hands it to the consumers through a 4-slot ring (the unit's
 //                q rows arrive by a 1-D bulk copy into the ring slot), then streams the
@@ -82,7 +83,7 @@ struct DecodeParams {
   float *part_o;
   float *part_lse;
   uint16_t *out;
-  int32_t *queue;
+  int32_t *queue;  // next unit to hand out; nullptr: CTA i takes unit i only
   unsigned int *err;
   int64_t num_blocks;
   int64_t cap;  // longest context the table rows and the split grid can address
@@ -131,11 +132,18 @@ __global__ void __maxnreg__(96)
     const uint64_t policy = policy_evict_first();
     uint32_t pushed = 0, tiles = 0;
     bool ok = true;
+    int static_next = blockIdx.x;  // without a queue: unit blockIdx.x, then nothing
     while (ok) {
       // next unit with work (or one that must write zeros); ntiles < 0 ends the walk
       Unit un{0, 0, 0, -1};
       while (true) {
-        const int u = atomicAdd(p.queue, 1);
+        int u;
+        if (p.queue) {
+          u = atomicAdd(p.queue, 1);
+        } else {
+          u = static_next;
+          static_next = p.units;
+        }
         if (u >= p.units) break;
         const int s = u / (p.batch * p.xgroups);
         const int r = u % (p.batch * p.xgroups);
@@ -556,7 +564,12 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &p, cudaSt
   prm.units = (int32_t)units;
   prm.qscale = a.scale * kLog2e;
 
-  cudaError_t e = cudaMemsetAsync(prm.queue, 0, sizeof(int32_t), stream);
+  // With no more units than CTAs each CTA takes unit blockIdx.x and the counter (and the
+  // memset that resets it) is not needed.
+  const bool queued = (int64_t)a.num_sms * 2 < units;
+  cudaError_t e = cudaSuccess;
+  if (queued) e = cudaMemsetAsync(prm.queue, 0, sizeof(int32_t), stream);
+  else prm.queue = nullptr;
   if (e != cudaSuccess) return e;
   e = p.heads_per_cta == 2 ? launch_split<2>(km, vm, prm, a.num_sms, stream)
                            : launch_split<1>(km, vm, prm, a.num_sms, stream);
