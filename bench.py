@@ -44,7 +44,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one decode_split_kernel launch on
 # the Qwen3 decode batch, from one ncu capture of the current kernel; None whenever the kernel
 # has changed since that capture.
-DECODE_SPLIT_DRAM_BYTES = 1_184_072_104
+DECODE_SPLIT_DRAM_BYTES = None
 FALLBACK_BF16_TFLOPS = 1900.0
 WORKLOAD = ("qwen3-0.6b decode step: 28 layers x (kv_store of 256 new tokens + paged decode "
             "attention), B=256, ctx U[100,2048] (seed 2), block_size 256, 16 q / 8 kv heads, "
@@ -198,21 +198,22 @@ class DecodeStep:
         pkv, s = self.pkv, self.pool
         io = io or {n: getattr(self, n) for n in self.IO + ("out",)}
         for l in range(self.layers):
-            pkv.kv_store(io["kn"][l], io["vn"][l], io["slots"], s[0, l], s[1, l])
             if events is not None:
                 events.append(torch.cuda.Event(enable_timing=True))
                 events[-1].record()
-            pkv.paged_decode_attn(io["q"][l], s[0, l], s[1, l], io["tables"], io["ctx"],
-                                  self.maxc, self.lay.scale, num_splits=self.num_splits,
-                                  workspace=self.ws, out=io["out"][l])
+            # the layer's new tokens stored and attended in one call
+            pkv.paged_decode_step(io["q"][l], io["kn"][l], io["vn"][l], io["slots"], s[0, l],
+                                  s[1, l], io["tables"], io["ctx"], self.maxc, self.lay.scale,
+                                  num_splits=self.num_splits, workspace=self.ws,
+                                  out=io["out"][l])
             if events is not None:
                 events.append(torch.cuda.Event(enable_timing=True))
                 events[-1].record()
 
     def launches_per_step(self):
-        # kv_store + split kernel, + the combine kernel when the context is split (the
-        # workspace then holds partial outputs beyond its 16-byte work counter)
-        return self.layers * (2 + (1 if self.splits_workspace > 16 else 0))
+        # the split kernel (which also stores the new tokens), + the combine kernel when the
+        # context is split (the workspace then holds partial outputs beyond its 16-byte counter)
+        return self.layers * (1 + (1 if self.splits_workspace > 16 else 0))
 
 
 def time_e2e(step: DecodeStep, steps: int):
@@ -571,7 +572,7 @@ def run_ours(args):
     if rank != 0:
         return
     total_bytes = step.step_bytes * world
-    dec_bytes = step.bytes["decode"]
+    dec_bytes = step.bytes["decode"] + step.bytes["store"]  # the call stores and attends
     achieved = dec_bytes / decode_avg / 1e9
     line = {
         "metric": METRIC,
@@ -593,7 +594,8 @@ def run_ours(args):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "kv_tokens_per_s": step.kv_tokens * world / per_step,
         "decode_frac_of_hbm_peak": achieved / hbm_peak,
-        "roofline": {"bound": "hbm", "kernel": "paged_decode_attn (split + combine)",
+        "roofline": {"bound": "hbm",
+                     "kernel": "paged_decode_step (split kernel with the store, + combine)",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "peak_source": peak_src,
                      "traffic": DECODE_SPLIT_DRAM_BYTES,
@@ -662,10 +664,10 @@ def run_profile(args):
         step = DecodeStep(pkv, num_blocks=w.blocks_needed(ctx) + 8, layers=1,
                           num_splits=args.num_splits)
         s = step.pool
-        run = lambda: pkv.paged_decode_attn(step.q[0], s[0, 0], s[1, 0], step.tables, step.ctx,
-                                            step.maxc, step.lay.scale,
-                                            num_splits=args.num_splits, workspace=step.ws,
-                                            out=step.out[0])
+        run = lambda: pkv.paged_decode_step(step.q[0], step.kn[0], step.vn[0], step.slots,
+                                            s[0, 0], s[1, 0], step.tables, step.ctx, step.maxc,
+                                            step.lay.scale, num_splits=args.num_splits,
+                                            workspace=step.ws, out=step.out[0])
     elif args.profile == "store":
         lens = w.varlen_prefill_lengths()
         lay = w.varlen_prefill_layout(num_blocks=w.blocks_needed(lens) + 64)

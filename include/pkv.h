@@ -157,6 +157,35 @@ pkv_status pkv_paged_decode_attn(const void *q, const void *k_cache, const void 
                                  void *stream);
 
 /*
+ * paged_decode_step -- one decode step of a layer in one call: each sequence's new token is
+ * written into the pools at slot_mapping[b] (as pkv_kv_store does: «nano-vLLM 最小化vLLM重新实现»,
+ * 架构 5, the store through slot_mapping) and then every sequence attends over its context
+ * (as pkv_paged_decode_attn, whose arguments and workspace these are). The store happens
+ * inside the decode kernel: the part of the kernel that reads a sequence's last position for
+ * a KV head writes that row first, so the step needs no separate store kernel (with more than
+ * one CTA per KV head -- num_q_heads / num_kv_heads >= 3 -- a store kernel runs first instead).
+ *
+ * k_new, v_new: [batch, num_kv_heads, head_dim] bf16, token strides in elements (multiples of
+ *               8); slot_mapping: [batch] int64. The new token of sequence b is position
+ *               context_lens[b] - 1 and slot_mapping[b] must be that position's slot in b's
+ *               block table; a negative slot stores nothing (a padding row). A sequence with
+ *               context length 0 stores nothing. A slot may not be read by another sequence
+ *               in the same call (new tokens go to a sequence's own blocks). Slot >=
+ *               num_blocks * block_size: skipped, PKV_DEVERR_SLOT_RANGE.
+ * The result equals pkv_kv_store followed by pkv_paged_decode_attn, bit for bit.
+ */
+pkv_status pkv_paged_decode_step(const void *q, const void *k_new, int64_t k_new_tok_stride,
+                                 const void *v_new, int64_t v_new_tok_stride,
+                                 const int64_t *slot_mapping, void *k_cache, void *v_cache,
+                                 const int32_t *block_tables, int32_t block_table_width,
+                                 const int32_t *context_lens, int32_t batch,
+                                 int32_t max_context_len, int32_t num_q_heads,
+                                 int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                 int64_t num_blocks, float scale, int32_t num_splits,
+                                 void *workspace, size_t workspace_bytes, void *out,
+                                 void *stream);
+
+/*
  * Bytes of device workspace that pkv_varlen_prefill_attn needs for num_seqs sequences of at
  * most max_seqlen_q queries: a 16-byte header (the persistent kernel's work counter and the
  * length of its work list), about 12 bytes per sequence and 8 per possible query-block count

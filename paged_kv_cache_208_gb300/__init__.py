@@ -36,6 +36,9 @@ SIGNATURES = {
                                      _I32, _I64, _F, _I32, _P, _SZ, _P, _P]),
     "pkv_paged_decode_attn_noalloc": (_I32, [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32,
                                              _I32, _I32, _I64, _F, _I32, _P, _P]),
+    "pkv_paged_decode_step": (_I32, [_P, _P, _I64, _P, _I64, _P, _P, _P, _P, _I32, _P, _I32,
+                                     _I32, _I32, _I32, _I32, _I32, _I64, _F, _I32, _P, _SZ,
+                                     _P, _P]),
     "pkv_prefill_workspace_bytes": (_SZ, [_I32, _I32, _I32, _I32]),
     "pkv_varlen_prefill_attn": (_I32, [_P, _I64, _I64, _P, _P, _I64, _I64, _P, _P, _I32, _I32,
                                        _I32, _P, _I32, _I32, _I64, _I32, _I32, _I32, _F, _I32,
@@ -170,6 +173,42 @@ def paged_decode_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
         workspace = decode_workspace(B, hq, hkv, d, max_context_len, num_splits, q.device)
     _check("pkv_paged_decode_attn", _LIB.pkv_paged_decode_attn(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+        _ptr(context_lens), B, int(max_context_len), hq, hkv, d, bs, nb, float(scale),
+        int(num_splits), _ptr(workspace), workspace.numel(), _ptr(out), _stream(stream)))
+    return out
+
+
+def paged_decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                      slot_mapping: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                      block_tables: torch.Tensor, context_lens: torch.Tensor,
+                      max_context_len: int, scale: float, num_splits: int = 0,
+                      workspace: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                      stream=None) -> torch.Tensor:
+    """Store each sequence's new token (k_new, v_new: [B, Hkv, D], rows may be strided views;
+    slot_mapping [B] int64) and attend, in one call: the same result as kv_store followed by
+    paged_decode_attn."""
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (k_new, "k_new"),
+                 (v_new, "v_new")):
+        _need(t, n, torch.bfloat16)
+    _need(block_tables, "block_tables", torch.int32)
+    _need(context_lens, "context_lens", torch.int32)
+    _need(slot_mapping, "slot_mapping", torch.int64)
+    if not (q.is_contiguous() and k_cache.is_contiguous() and v_cache.is_contiguous()
+            and block_tables.is_contiguous() and context_lens.is_contiguous()
+            and slot_mapping.is_contiguous()):
+        raise ValueError("q, caches, block_tables, context_lens, slot_mapping must be contiguous")
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        if t.stride(-1) != 1 or t.stride(-2) != t.shape[-1]:
+            raise ValueError(f"{n}: each token's heads must be dense")
+    B, hq, d = q.shape
+    nb, bs, hkv, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = decode_workspace(B, hq, hkv, d, max_context_len, num_splits, q.device)
+    _check("pkv_paged_decode_step", _LIB.pkv_paged_decode_step(
+        _ptr(q), _ptr(k_new), k_new.stride(0), _ptr(v_new), v_new.stride(0), _ptr(slot_mapping),
+        _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
         _ptr(context_lens), B, int(max_context_len), hq, hkv, d, bs, nb, float(scale),
         int(num_splits), _ptr(workspace), workspace.numel(), _ptr(out), _stream(stream)))
     return out

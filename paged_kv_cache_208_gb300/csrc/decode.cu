@@ -51,6 +51,7 @@ constexpr unsigned kFull = 0xffffffffu;
 
 struct Unit {
   int32_t b, s, xg, ntiles;  // ntiles < 0: no more work
+  int32_t store;             // store the sequence's new token (its last position) first
 };
 
 template <int GC>
@@ -61,10 +62,12 @@ struct DecodeSmem {
   float m[kConsumerWarps][GC];
   float l[kConsumerWarps][GC];
   uint16_t qs[kRing][GC][kD];  // q rows of the queued units
+  alignas(16) uint16_t newkv[kRing][2][kD];  // a unit's new K and V rows, bound for the pool
   Unit unit[kRing];
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t unit_full[kRing];
+  uint64_t newkv_full[kRing];
   uint64_t unit_empty[kRing];
 };
 
@@ -98,6 +101,15 @@ struct DecodeParams {
   int32_t splits;
   int32_t units;    // splits * batch * xgroups
   float qscale;
+  // the step's new tokens (k_new == nullptr: nothing to store)
+  const uint16_t *k_new;
+  const uint16_t *v_new;
+  int64_t k_new_stride, v_new_stride;  // elements per token
+  const int64_t *slots;
+  int64_t num_slots;
+  uint16_t *k_cache_w;
+  uint16_t *v_cache_w;
+  int32_t num_kv_heads;
 };
 
 template <int GC>
@@ -118,6 +130,7 @@ __global__ void __maxnreg__(96)
     }
     for (int i = 0; i < kRing; ++i) {
       mbar_init(&sm.unit_full[i], 1);
+      mbar_init(&sm.newkv_full[i], 1);
       mbar_init(&sm.unit_empty[i], kConsumerWarps);
     }
     fence_mbar_init();
@@ -133,9 +146,12 @@ __global__ void __maxnreg__(96)
     uint32_t pushed = 0, tiles = 0;
     bool ok = true;
     int static_next = blockIdx.x;  // without a queue: unit blockIdx.x, then nothing
+    uint32_t newkv_par = 0;        // bit s: parity of newkv_full[s]'s next phase
+    bool newkv_pending = false;    // new-token rows on their way into shared memory
+    int newkv_slot = 0;
     while (ok) {
       // next unit with work (or one that must write zeros); ntiles < 0 ends the walk
-      Unit un{0, 0, 0, -1};
+      Unit un{0, 0, 0, -1, 0};
       while (true) {
         int u;
         if (p.queue) {
@@ -156,11 +172,14 @@ __global__ void __maxnreg__(96)
         const int64_t begin = (int64_t)s * p.chunk;
         if (begin < L) {
           const int64_t end = min(L, begin + p.chunk);
-          un = Unit{b, s, xg, (int)((end - begin + kTile - 1) / kTile)};
+          // the unit that reads position L - 1 stores the new token there first (only one
+          // unit per KV head reads it: the launcher takes this path with one head group)
+          un = Unit{b, s, xg, (int)((end - begin + kTile - 1) / kTile),
+                    p.k_new != nullptr && end == L ? 1 : 0};
           break;
         }
         if (L == 0 && s == 0 && p.splits == 1) {  // empty context, direct output: zeros
-          un = Unit{b, s, xg, 0};
+          un = Unit{b, s, xg, 0, 0};
           break;
         }
       }
@@ -181,6 +200,24 @@ __global__ void __maxnreg__(96)
       mbar_arrive_expect_tx(&sm.unit_full[slot], GC * kD * 2);
       bulk_copy_g2s(sm.qs[slot], p.q + ((int64_t)un.b * p.num_q_heads + hq0) * kD, GC * kD * 2,
                     &sm.unit_full[slot]);
+      // the unit that reads the context's last position brings the new token's K and V rows
+      // of its head into shared memory now (the pool write happens before its last tile)
+      uint16_t *store_dst = nullptr, *store_dst_v = nullptr;
+      if (un.store) {
+        const int64_t sl = p.slots[un.b];
+        if (sl >= p.num_slots) record_error(p.err, 1u /* SLOT_RANGE */);
+        if (sl >= 0 && sl < p.num_slots) {
+          store_dst = p.k_cache_w + (sl * p.num_kv_heads + h) * kD;
+          store_dst_v = p.v_cache_w + (sl * p.num_kv_heads + h) * kD;
+          mbar_arrive_expect_tx(&sm.newkv_full[slot], 2 * kD * 2);
+          bulk_copy_g2s(sm.newkv[slot][0], p.k_new + un.b * p.k_new_stride + h * kD, kD * 2,
+                        &sm.newkv_full[slot]);
+          bulk_copy_g2s(sm.newkv[slot][1], p.v_new + un.b * p.v_new_stride + h * kD, kD * 2,
+                        &sm.newkv_full[slot]);
+          newkv_pending = true;
+          newkv_slot = slot;
+        }
+      }
       const int32_t *table = p.block_tables + (int64_t)un.b * p.table_width;
       const int tok_begin = un.s * p.chunk;
       for (int it = 0; it < un.ntiles; ++it, ++tiles) {
@@ -188,6 +225,22 @@ __global__ void __maxnreg__(96)
         if (tiles >= kStages && !wait_parity(&sm.empty[stage], ((tiles / kStages) - 1) & 1, p.err)) {
           ok = false;
           break;
+        }
+        if (store_dst && it == un.ntiles - 1) {
+          // This tile holds the context's last position: the new token's rows must be in the
+          // pool before its TMA load. They arrived in shared memory at the unit's start; copy
+          // them out with the bulk engine and wait for the writes (all in the async proxy, so
+          // the load below is ordered after them).
+          if (!wait_parity(&sm.newkv_full[slot], (newkv_par >> slot) & 1, p.err)) {
+            ok = false;
+            break;
+          }
+          newkv_par ^= 1u << slot;
+          newkv_pending = false;
+          bulk_copy_s2g(store_dst, sm.newkv[slot][0], kD * 2);
+          bulk_copy_s2g(store_dst_v, sm.newkv[slot][1], kD * 2);
+          bulk_commit();
+          bulk_wait_all();
         }
         const int pos = tok_begin + it * kTile;
         const int64_t blk = table[pos / p.block_size];
@@ -205,6 +258,7 @@ __global__ void __maxnreg__(96)
     }
     // keep the CTA alive until every copy it issued has landed
     bool drained = true;
+    if (newkv_pending) drained = wait_parity(&sm.newkv_full[newkv_slot], (newkv_par >> newkv_slot) & 1, p.err);
     for (uint32_t t = tiles > kStages ? tiles - kStages : 0; drained && t < tiles; ++t)
       drained = wait_parity(&sm.full[t % kStages], (t / kStages) & 1, p.err);
     for (uint32_t k = pushed > kRing ? pushed - kRing : 0; drained && k < pushed; ++k)
@@ -563,6 +617,25 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &p, cudaSt
   if (units > INT32_MAX) return cudaErrorInvalidValue;
   prm.units = (int32_t)units;
   prm.qscale = a.scale * kLog2e;
+  prm.num_kv_heads = a.num_kv_heads;
+  if (a.k_new) {
+    if (p.head_groups == 1) {  // each KV head's last position is read by one unit: fused
+      prm.k_new = static_cast<const uint16_t *>(a.k_new);
+      prm.v_new = static_cast<const uint16_t *>(a.v_new);
+      prm.k_new_stride = a.k_new_stride;
+      prm.v_new_stride = a.v_new_stride;
+      prm.slots = a.slot_mapping;
+      prm.num_slots = a.num_slots;
+      prm.k_cache_w = static_cast<uint16_t *>(const_cast<void *>(a.k_cache));
+      prm.v_cache_w = static_cast<uint16_t *>(const_cast<void *>(a.v_cache));
+    } else {  // several CTAs read one head's rows: store first, as a kernel of its own
+      cudaError_t e = launch_kv_store(a.k_new, a.k_new_stride, a.v_new, a.v_new_stride,
+                                      a.slot_mapping, a.batch, const_cast<void *>(a.k_cache),
+                                      const_cast<void *>(a.v_cache), a.num_slots,
+                                      (int64_t)a.num_kv_heads * kD, a.err, a.num_sms, stream);
+      if (e != cudaSuccess) return e;
+    }
+  }
 
   // With no more units than CTAs each CTA takes unit blockIdx.x and the counter (and the
   // memset that resets it) is not needed.

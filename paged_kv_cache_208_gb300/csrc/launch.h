@@ -45,6 +45,14 @@ struct DecodeArgs {
   void *out;
   unsigned int *err;
   int num_sms;
+  // optional: the step's new tokens, stored into the pools before they are read (one per
+  // sequence, [batch, num_kv_heads, 128] with these token strides, at slot_mapping[b])
+  const void *k_new = nullptr;
+  const void *v_new = nullptr;
+  int64_t k_new_stride = 0;
+  int64_t v_new_stride = 0;
+  const int64_t *slot_mapping = nullptr;
+  int64_t num_slots = 0;
 };
 constexpr size_t kDecodeQueueBytes = 16;  // the persistent kernel's work counter
 cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &plan,

@@ -193,6 +193,51 @@ pkv_status pkv_paged_decode_attn(const void *q, const void *k_cache, const void 
   return launch_status(pkv::launch_paged_decode(a, plan, static_cast<cudaStream_t>(stream)));
 }
 
+pkv_status pkv_paged_decode_step(const void *q, const void *k_new, int64_t k_new_tok_stride,
+                                 const void *v_new, int64_t v_new_tok_stride,
+                                 const int64_t *slot_mapping, void *k_cache, void *v_cache,
+                                 const int32_t *block_tables, int32_t block_table_width,
+                                 const int32_t *context_lens, int32_t batch,
+                                 int32_t max_context_len, int32_t num_q_heads,
+                                 int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                 int64_t num_blocks, float scale, int32_t num_splits,
+                                 void *workspace, size_t workspace_bytes, void *out,
+                                 void *stream) {
+  if (batch < 0 || max_context_len < 0 || num_splits < 0 || num_q_heads <= 0 ||
+      num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || head_dim <= 0 ||
+      block_size <= 0 || num_blocks <= 0 || block_table_width <= 0 || !isfinite(scale))
+    return PKV_ERR_INVALID_ARG;
+  const int64_t row = (int64_t)num_kv_heads * head_dim;
+  if (k_new_tok_stride < row || v_new_tok_stride < row) return PKV_ERR_INVALID_ARG;
+  if (batch == 0) return PKV_OK;
+  if (!q || !k_new || !v_new || !slot_mapping || !k_cache || !v_cache || !block_tables ||
+      !context_lens || !out)
+    return PKV_ERR_INVALID_ARG;
+  if (head_dim != 128 || block_size % 256 != 0) return PKV_ERR_UNSUPPORTED;
+  if (num_blocks * (int64_t)block_size > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      !aligned16(k_new) || !aligned16(v_new) || k_new_tok_stride % 8 != 0 ||
+      v_new_tok_stride % 8 != 0)
+    return PKV_ERR_UNSUPPORTED;
+  DeviceInfo *dev = device_info();
+  if (!dev) return PKV_ERR_CUDA;
+  const pkv::DecodePlan plan = pkv::plan_decode(batch, num_q_heads, num_kv_heads,
+                                                max_context_len, num_splits, dev->num_sms);
+  if (!workspace || workspace_bytes < plan.workspace_bytes || !aligned16(workspace))
+    return PKV_ERR_WORKSPACE;
+  pkv::DecodeArgs a{q,           k_cache,        v_cache,      block_tables, block_table_width,
+                    context_lens, batch,          num_q_heads,  num_kv_heads, block_size,
+                    num_blocks,  scale,          workspace,    out,          dev->err,
+                    dev->num_sms};
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.k_new_stride = k_new_tok_stride;
+  a.v_new_stride = v_new_tok_stride;
+  a.slot_mapping = slot_mapping;
+  a.num_slots = num_blocks * block_size;
+  return launch_status(pkv::launch_paged_decode(a, plan, static_cast<cudaStream_t>(stream)));
+}
+
 size_t pkv_prefill_workspace_bytes(int32_t num_seqs, int32_t max_seqlen_q, int32_t num_q_heads,
                                    int32_t head_dim) {
   if (num_seqs < 0 || max_seqlen_q < 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
