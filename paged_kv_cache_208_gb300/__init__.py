@@ -268,6 +268,10 @@ def varlen_prefill_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
         kv_stride, nb, bs, W = k.stride(0), 0, 0, 0
     if out is None:
         out = torch.empty((tq, hq, d), dtype=q.dtype, device=q.device)
+    else:
+        _need(out, "out", torch.bfloat16)
+        if tuple(out.shape) != (tq, hq, d) or not out.is_contiguous():
+            raise ValueError("out must be a contiguous [Tq, Hq, D] tensor")
     n = cu_seqlens_q.shape[0] - 1
     if workspace is None:
         workspace = torch.empty(max(16, int(_LIB.pkv_prefill_workspace_bytes(n, int(max_seqlen_q),

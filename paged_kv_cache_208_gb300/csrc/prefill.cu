@@ -115,6 +115,7 @@ struct PrefillParams {
   float scale_log2;
   int32_t causal;
   uint16_t *out;
+  bool out_32b;    // out is 32-byte aligned: rows are written with 32-byte stores
   int32_t *queue;  // next item to hand out (zeroed before the launch)
   unsigned int *err;
 };
@@ -219,6 +220,13 @@ __device__ __forceinline__ void mma_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_
 __device__ __forceinline__ void commit_one(uint64_t *bar) {
   if (elect_one()) umma_commit(bar);
   __syncwarp();
+}
+
+// One 32-byte global store (sm_100 and later); p must be 32-byte aligned.
+__device__ __forceinline__ void st_global_32b(void *p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -603,14 +611,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(lane_addr + o_col + 32 * c, o);
         tmem_ld_wait(o);
         if (row_valid) {
+          // a thread writes its own row: one 32-byte sector per store when out allows it
+          // (a warp's store touches 32 rows, so fewer and wider stores leave the load/store
+          // queue free sooner for the TMEM, shared-memory and UMMA traffic behind them)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            uint4 v4;
-            v4.x = pack_bf16(__uint_as_float(o[8 * e + 0]) * inv, __uint_as_float(o[8 * e + 1]) * inv);
-            v4.y = pack_bf16(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv);
-            v4.z = pack_bf16(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv);
-            v4.w = pack_bf16(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv);
-            dst[c * 4 + e] = v4;
+          for (int e = 0; e < 2; ++e) {
+            uint32_t w[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              w[k] = pack_bf16(__uint_as_float(o[16 * e + 2 * k]) * inv,
+                               __uint_as_float(o[16 * e + 2 * k + 1]) * inv);
+            uint4 *d = dst + c * 4 + 2 * e;
+            if (p.out_32b) {
+              st_global_32b(d, w);
+            } else {
+              d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+              d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            }
           }
         }
       }
@@ -820,6 +837,7 @@ cudaError_t launch_varlen_prefill(const PrefillArgs &a, int num_sms, cudaStream_
   prm.scale_log2 = a.scale * kLog2e;
   prm.causal = a.causal;
   prm.out = static_cast<uint16_t *>(a.out);
+  prm.out_32b = (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0;
   prm.err = a.err;
   switch (a.num_q_heads / a.num_kv_heads) {
     case 1: return launch_g<1>(a, prm, num_sms, stream);

@@ -56,6 +56,23 @@ def test_prefill_head_groupings(hq, hkv):
     assert_attention_close(_run(q, k, v, cq, ck), ref, f"hq={hq} hkv={hkv}")
 
 
+def test_prefill_out_aligned_to_16_bytes_only():
+    """An out buffer that starts 16 bytes past a 32-byte boundary takes the 16-byte store
+    path: the same values as an aligned out, bit for bit, and no byte outside it written."""
+    q, k, v, cq, ck = _case([300, 5, 129], seed=41)
+    aligned = _run(q, k, v, cq, ck)
+    n = aligned.numel()
+    big = torch.full((n + 32,), -7.0, dtype=torch.bfloat16, device="cuda")
+    out = big[8:8 + n].view(aligned.shape)  # 8 bf16 = 16 bytes past the start
+    assert out.data_ptr() % 32 == 16
+    lq = np.diff(cq)
+    pkv.varlen_prefill_attn(dev(q), dev(k), dev(v), dev(cq), dev(ck), int(lq.max()),
+                            int(lq.max()), 128 ** -0.5, out=out)
+    assert torch.equal(out.view(torch.int16), aligned.view(torch.int16))
+    assert (big[:8] == -7.0).all() and (big[8 + n:] == -7.0).all()
+    assert pkv.get_device_errors() == 0
+
+
 def test_prefill_non_causal_and_unequal_lengths():
     q, k, v, cq, ck = _case([100, 37], seed=5, lens_k=[300, 129])
     for causal in (False, True):
