@@ -173,17 +173,19 @@ __device__ __forceinline__ Item decode_item(const PrefillParams &p, int i) {
 
 // Next work item from the ring (in order), taken by a whole warp: every lane waits, and the
 // item counts only if every lane saw it (so the warp agrees even when a wait gives up).
-// it.id < 0 at the end of the work, or when the wait gave up. The caller releases the slot
-// (item_empty) after copying the item.
-__device__ __forceinline__ Item take_item(PrefillSmem &sm, uint32_t taken, unsigned int *err) {
+// Returns the slot, or nullptr when the wait gave up. The caller reads the fields it needs
+// in place and then releases the slot (release_item).
+__device__ __forceinline__ const Item *wait_item(PrefillSmem &sm, uint32_t taken,
+                                                 unsigned int *err) {
   const int slot = taken % kRing;
-  Item it;
-  if (__all_sync(0xffffffffu, wait_parity(&sm.item_full[slot], (taken / kRing) & 1, err))) {
-    it = sm.items[slot];
-  } else {
-    it.id = -1;
-  }
-  return it;
+  if (__all_sync(0xffffffffu, wait_parity(&sm.item_full[slot], (taken / kRing) & 1, err)))
+    return &sm.items[slot];
+  return nullptr;
+}
+
+__device__ __forceinline__ void release_item(PrefillSmem &sm, uint32_t taken, int lane) {
+  __syncwarp();  // every lane has read the item before the slot is released
+  if (lane == 0) mbar_arrive(&sm.item_empty[taken % kRing]);
 }
 
 // S = Q K^T for one 128 x 128 tile: 8 UMMAs of K = 16 over the two 64-column halves. The
@@ -428,14 +430,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       return wait_all(&sm.kv_full[vs], (n / kSlots) & 1);
     };
     while (ok) {
-      Item it = take_item(sm, taken, p.err);
-      __syncwarp();  // every lane has copied the item before the slot is released
-      if (lane == 0) mbar_arrive(&sm.item_empty[taken % kRing]);
+      const Item *ip = wait_item(sm, taken, p.err);
+      const int id = ip ? ip->id : -1, nk = ip ? ip->nk : 0;
+      const bool fix_v = ip && ip->last_rows < kBN;
+      release_item(sm, taken, lane);
       ++taken;
-      if (it.id < 0) break;
-      if (it.nk == 0) continue;
-      const int nk = it.nk;
-      const bool fix_v = it.last_rows < kBN;
+      if (id < 0) break;
+      if (nk == 0) continue;
       for (int j = 0; j < nk; ++j, ++g) {
         const uint32_t ks = (2 * g) % kSlots;
         ok = wait_all(&sm.kv_full[ks], ((2 * g) / kSlots) & 1);
@@ -503,24 +504,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t taken = 0, g = 0;
     bool ok = true;
     while (ok) {
-      Item it = take_item(sm, taken, p.err);
-      __syncwarp();  // every lane has copied the item before the slot is released
-      if (lane == 0) mbar_arrive(&sm.item_empty[taken % kRing]);
+      const Item *ip = wait_item(sm, taken, p.err);
+      const int id = ip ? ip->id : -1, nk = ip ? ip->nk : 0;
+      int64_t row = -1;  // output row (token x head) of this thread; -1 past the queries
+      int64_t lim = -1;  // last key this row sees (-1: none)
+      if (id >= 0) {
+        const int64_t qi = ip->tok[a] + r, Lq = ip->Lq, Lk = ip->Lk;
+        if (qi < Lq) {
+          row = (ip->q0 + qi) * p.num_q_heads + ip->hq[a];
+          lim = min(p.causal ? qi + (Lk - Lq) : Lk - 1, Lk - 1);
+        }
+      }
+      release_item(sm, taken, lane);
       ++taken;
-      if (it.id < 0) break;
-      const int64_t qi = it.tok[a] + r;
-      const bool row_valid = qi < it.Lq;
-      uint4 *dst = reinterpret_cast<uint4 *>(
-          p.out + ((it.q0 + qi) * p.num_q_heads + it.hq[a]) * kD);
-      if (it.nk == 0) {  // no key is visible to any row: zeros
+      if (id < 0) break;
+      const bool row_valid = row >= 0;
+      uint4 *dst = reinterpret_cast<uint4 *>(p.out + (row_valid ? row : 0) * kD);
+      if (nk == 0) {  // no key is visible to any row: zeros
         if (row_valid)
           for (int c = 0; c < 16; ++c) dst[c] = make_uint4(0, 0, 0, 0);
         continue;
       }
-      int64_t lim = !row_valid ? -1 : (p.causal ? qi + (it.Lk - it.Lq) : it.Lk - 1);
-      if (lim > it.Lk - 1) lim = it.Lk - 1;
       float m_run = -INFINITY, l_run = 0.f;
-      for (int j = 0; j < it.nk; ++j, ++g) {
+      for (int j = 0; j < nk; ++j, ++g) {
         // warp-uniform results: the TMEM loads and stores below are .sync.aligned
         ok = __all_sync(kFull, wait_parity(&sm.s_full[a], g & 1, p.err));
         if (!ok) break;
