@@ -17,9 +17,9 @@
 //
 // A quarter warp (8 lanes) owns a head row: lane l holds elements 8l..8l+7 and their RoPE
 // partners 64+8l..64+8l+7 (16-byte loads and stores), so the rotation needs no exchange and
-// the sum of squares takes three shuffles. A warp does eight rows, two per quarter; HBM
-// traffic per token is its projection row in and q, K and V out. Roundings to bf16 go two
-// values per conversion instruction.
+// the sum of squares takes three shuffles. A warp does eight consecutive heads of one token,
+// two per quarter; HBM traffic per token is its projection row in and q, K and V out.
+// Roundings to bf16 go two values per conversion instruction.
 #include <math.h>
 #include <stdint.h>
 
@@ -92,11 +92,12 @@ struct Row {
   float ss;
 };
 
-__device__ __forceinline__ Row load_row(const RopeParams &p, int64_t row, int heads, int gl) {
+__device__ __forceinline__ Row load_row(const RopeParams &p, int64_t t, int h, int heads,
+                                        int gl) {
   Row r;
-  r.live = row < p.num_tokens * heads;
-  r.t = r.live ? row / heads : 0;
-  r.h = r.live ? (int)(row % heads) : 0;
+  r.live = t < p.num_tokens && h < heads;
+  r.t = r.live ? t : 0;
+  r.h = r.live ? h : 0;
   const uint16_t *src = p.qkv + r.t * p.tok_stride + (int64_t)r.h * kD;
   r.lo = r.live ? ld_stream_u4(reinterpret_cast<const uint4 *>(src + 8 * gl))
                 : make_uint4(0, 0, 0, 0);
@@ -168,16 +169,19 @@ __device__ __forceinline__ float sum_sq(const uint4 lo, const uint4 hi) {
   return ss;
 }
 
-// A quarter warp owns two head rows (base + g and base + 4 + g of the warp's eight): all
-// four 16-byte loads are issued before any arithmetic, so each lane keeps 64 bytes in flight.
-__global__ void __launch_bounds__(kThreads) qk_norm_rope_store_kernel(const RopeParams p) {
+// A warp owns eight consecutive heads of one token; quarter warp g takes heads 8k + g and
+// 8k + 4 + g. All four 16-byte loads are issued before any arithmetic, so each lane keeps 64
+// bytes in flight. The token and head block come from one 32-bit division per warp.
+__global__ void __launch_bounds__(kThreads, 4) qk_norm_rope_store_kernel(const RopeParams p,
+                                                                       uint32_t warps_per_token) {
   const int lane = threadIdx.x & 31;
   const int group = lane >> 3, gl = lane & 7;
   const int heads = p.hq + 2 * p.hkv;
-  const int64_t base = ((int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) *
-                       (kRowsPerQuarter * kRowsPerWarp);
-  Row r0 = load_row(p, base + group, heads, gl);
-  Row r1 = load_row(p, base + kRowsPerWarp + group, heads, gl);
+  const uint32_t wg = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+  const uint32_t t = wg / warps_per_token;
+  const int h0 = (int)(wg - t * warps_per_token) * (kRowsPerQuarter * kRowsPerWarp) + group;
+  Row r0 = load_row(p, t, h0, heads, gl);
+  Row r1 = load_row(p, t, h0 + kRowsPerWarp, heads, gl);
   r0.ss = sum_sq(r0.lo, r0.hi);
   r1.ss = sum_sq(r1.lo, r1.hi);
   // each quarter warp's sums (lanes 8g..8g+7); every lane of the warp takes part
@@ -218,10 +222,11 @@ extern "C" pkv_status pkv_qk_norm_rope_store(
     return PKV_ERR_UNSUPPORTED;
   unsigned int *err = current_error_word();
   if (!err) return PKV_ERR_CUDA;
-  const int64_t rows = num_tokens * (num_q_heads + 2 * num_kv_heads);
-  const int64_t rows_per_cta = (kThreads / 32) * kRowsPerQuarter * kRowsPerWarp;
-  const int64_t grid = (rows + rows_per_cta - 1) / rows_per_cta;
-  if (grid > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  const int64_t rows_per_warp = kRowsPerQuarter * kRowsPerWarp;
+  const int64_t warps_per_token = (num_q_heads + 2 * num_kv_heads + rows_per_warp - 1) / rows_per_warp;
+  const int64_t warps = num_tokens * warps_per_token;
+  const int64_t grid = (warps + kThreads / 32 - 1) / (kThreads / 32);
+  if (grid * (kThreads / 32) > UINT32_MAX || grid > INT32_MAX) return PKV_ERR_UNSUPPORTED;
   RopeParams prm{};
   prm.qkv = static_cast<const uint16_t *>(qkv);
   prm.tok_stride = qkv_tok_stride;
@@ -241,6 +246,6 @@ extern "C" pkv_status pkv_qk_norm_rope_store(
   prm.hkv = num_kv_heads;
   prm.err = err;
   qk_norm_rope_store_kernel<<<(unsigned)grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-      prm);
+      prm, (uint32_t)warps_per_token);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
