@@ -15,12 +15,17 @@
 // with c = cos_sin[pos, 0:64], s = cos_sin[pos, 64:128], rounded to bf16 (RNE): query heads
 // to q_out, key heads to k_cache[slot]; value heads are copied to v_cache[slot] bit for bit.
 //
-// A quarter warp (8 lanes) owns a head row: lane l holds elements 8l..8l+7 and their RoPE
-// partners 64+8l..64+8l+7 (16-byte loads and stores), so the rotation needs no exchange and
-// the sum of squares takes three shuffles. A warp does eight consecutive heads of one token,
-// two per quarter; HBM traffic per token is its projection row in and q, K and V out.
-// Roundings to bf16 go two values per conversion instruction.
+// A warp owns one token. Its lane 0 brings the whole projection row (contiguous, 8 KiB for
+// 16 + 2 x 8 heads) into shared memory with one 1-D bulk copy, so a CTA keeps eight rows in
+// flight with no registers held for them. The warp then normalises and rotates the query and
+// key heads in place, eight rows at a time: a quarter warp (8 lanes) owns a head row, lane l
+// holding elements 8l..8l+7 and their RoPE partners 64+8l..64+8l+7, so the rotation needs no
+// exchange and the sum of squares takes three shuffles. Lane 0 then writes the token's q
+// heads, K heads and (untouched) V heads out with three bulk copies: q_out[t], and the
+// pool rows of slot[t]. Roundings to bf16 go two values per conversion instruction.
 #include <math.h>
+
+#include <algorithm>
 #include <stdint.h>
 
 #include <cuda_bf16.h>
@@ -34,9 +39,9 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kHalf = kD / 2;
-constexpr int kThreads = 256;
-constexpr int kRowsPerWarp = 4;     // quarter warps
-constexpr int kRowsPerQuarter = 2;  // head rows each quarter warp processes
+constexpr int kRowBytes = kD * 2;     // one head row, bf16
+constexpr int kMaxTokensPerCta = 8;   // one warp per token
+constexpr int kMaxSmem = 96 * 1024;   // staged projection rows per CTA (two CTAs per SM)
 
 struct RopeParams {
   const uint16_t *qkv;
@@ -84,81 +89,6 @@ __device__ __forceinline__ void round8(float (&f)[8]) {
   }
 }
 
-struct Row {
-  bool live;
-  int64_t t;
-  int h;
-  uint4 lo, hi;
-  float ss;
-};
-
-__device__ __forceinline__ Row load_row(const RopeParams &p, int64_t t, int h, int heads,
-                                        int gl) {
-  Row r;
-  r.live = t < p.num_tokens && h < heads;
-  r.t = r.live ? t : 0;
-  r.h = r.live ? h : 0;
-  const uint16_t *src = p.qkv + r.t * p.tok_stride + (int64_t)r.h * kD;
-  r.lo = r.live ? ld_stream_u4(reinterpret_cast<const uint4 *>(src + 8 * gl))
-                : make_uint4(0, 0, 0, 0);
-  r.hi = r.live ? ld_stream_u4(reinterpret_cast<const uint4 *>(src + kHalf + 8 * gl))
-                : make_uint4(0, 0, 0, 0);
-  return r;
-}
-
-// One head row after its sum of squares is known (no shuffles from here on).
-__device__ __forceinline__ void finish_row(const RopeParams &p, const Row &r, int gl) {
-  if (!r.live) return;
-  const bool is_v = r.h >= p.hq + p.hkv, is_q = r.h < p.hq;
-  const int64_t slot = is_q ? -1 : p.slots[r.t];
-  const bool slot_ok = slot >= 0 && slot < p.num_slots;
-  if (!is_q && slot >= p.num_slots && gl == 0) record_error(p.err, 1u /* SLOT_RANGE */);
-  if (is_v) {  // value head: straight copy
-    if (slot_ok) {
-      uint16_t *dst =
-          p.v_cache + slot * ((int64_t)p.hkv * kD) + (int64_t)(r.h - p.hq - p.hkv) * kD;
-      reinterpret_cast<uint4 *>(dst + 8 * gl)[0] = r.lo;
-      reinterpret_cast<uint4 *>(dst + kHalf + 8 * gl)[0] = r.hi;
-    }
-    return;
-  }
-  const int64_t pos = p.positions[r.t];
-  if (pos < 0 || pos >= p.max_position) {
-    if (gl == 0) record_error(p.err, 32u /* POSITION_RANGE */);
-    return;
-  }
-  if (!is_q && !slot_ok) return;
-  const float rs = rsqrtf(r.ss * (1.f / kD) + p.eps);
-  const uint16_t *wsrc = is_q ? p.q_weight : p.k_weight;
-  float a[8], b[8], wa[8], wb[8];
-  unpack8(r.lo, a);
-  unpack8(r.hi, b);
-  unpack8(*reinterpret_cast<const uint4 *>(wsrc + 8 * gl), wa);
-  unpack8(*reinterpret_cast<const uint4 *>(wsrc + kHalf + 8 * gl), wb);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    a[i] = a[i] * rs * wa[i];
-    b[i] = b[i] * rs * wb[i];
-  }
-  round8(a);
-  round8(b);
-  const float4 *cs = reinterpret_cast<const float4 *>(p.cos_sin + pos * kD);
-  const float4 c0 = cs[2 * gl], c1 = cs[2 * gl + 1];
-  const float4 s0 = cs[16 + 2 * gl], s1 = cs[16 + 2 * gl + 1];
-  const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-  const float s[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-  float ya[8], yb[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    ya[i] = a[i] * c[i] - b[i] * s[i];
-    yb[i] = b[i] * c[i] + a[i] * s[i];
-  }
-  uint16_t *dst = is_q ? p.q_out + (r.t * p.hq + r.h) * kD
-                       : p.k_cache + slot * ((int64_t)p.hkv * kD) + (int64_t)(r.h - p.hq) * kD;
-  reinterpret_cast<uint4 *>(dst + 8 * gl)[0] = pack8(ya);
-  reinterpret_cast<uint4 *>(dst + kHalf + 8 * gl)[0] = pack8(yb);
-}
-
 __device__ __forceinline__ float sum_sq(const uint4 lo, const uint4 hi) {
   float a[8], b[8];
   unpack8(lo, a);
@@ -169,29 +99,108 @@ __device__ __forceinline__ float sum_sq(const uint4 lo, const uint4 hi) {
   return ss;
 }
 
-// A warp owns eight consecutive heads of one token; quarter warp g takes heads 8k + g and
-// 8k + 4 + g. All four 16-byte loads are issued before any arithmetic, so each lane keeps 64
-// bytes in flight. The token and head block come from one 32-bit division per warp.
-__global__ void __launch_bounds__(kThreads, 4) qk_norm_rope_store_kernel(const RopeParams p,
-                                                                       uint32_t warps_per_token) {
-  const int lane = threadIdx.x & 31;
+// Normalise and rotate one head row held by a quarter warp (lo, hi: this lane's 8 + 8
+// elements), once its sum of squares is known; the result goes back over the row.
+__device__ __forceinline__ void finish_row(const RopeParams &p, uint8_t *row, uint4 lo, uint4 hi,
+                                           float ss, bool is_q, const float4 (&cs)[4], int gl) {
+  const float rs = rsqrtf(ss * (1.f / kD) + p.eps);
+  const uint16_t *wsrc = is_q ? p.q_weight : p.k_weight;
+  float a[8], b[8], wa[8], wb[8];
+  unpack8(lo, a);
+  unpack8(hi, b);
+  unpack8(*reinterpret_cast<const uint4 *>(wsrc + 8 * gl), wa);
+  unpack8(*reinterpret_cast<const uint4 *>(wsrc + kHalf + 8 * gl), wb);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    a[i] = a[i] * rs * wa[i];
+    b[i] = b[i] * rs * wb[i];
+  }
+  round8(a);
+  round8(b);
+  const float c[8] = {cs[0].x, cs[0].y, cs[0].z, cs[0].w, cs[1].x, cs[1].y, cs[1].z, cs[1].w};
+  const float s[8] = {cs[2].x, cs[2].y, cs[2].z, cs[2].w, cs[3].x, cs[3].y, cs[3].z, cs[3].w};
+  float ya[8], yb[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    ya[i] = a[i] * c[i] - b[i] * s[i];
+    yb[i] = b[i] * c[i] + a[i] * s[i];
+  }
+  reinterpret_cast<uint4 *>(row)[gl] = pack8(ya);
+  reinterpret_cast<uint4 *>(row + kHalf * 2)[gl] = pack8(yb);
+}
+
+__global__ void __launch_bounds__(kMaxTokensPerCta * 32)
+    qk_norm_rope_store_kernel(const RopeParams p, int tokens_per_cta) {
+  extern __shared__ __align__(128) uint8_t rows[];  // tokens_per_cta staged projection rows
+  __shared__ uint64_t row_full[kMaxTokensPerCta];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int group = lane >> 3, gl = lane & 7;
   const int heads = p.hq + 2 * p.hkv;
-  const uint32_t wg = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
-  const uint32_t t = wg / warps_per_token;
-  const int h0 = (int)(wg - t * warps_per_token) * (kRowsPerQuarter * kRowsPerWarp) + group;
-  Row r0 = load_row(p, t, h0, heads, gl);
-  Row r1 = load_row(p, t, h0 + kRowsPerWarp, heads, gl);
-  r0.ss = sum_sq(r0.lo, r0.hi);
-  r1.ss = sum_sq(r1.lo, r1.hi);
-  // each quarter warp's sums (lanes 8g..8g+7); every lane of the warp takes part
-#pragma unroll
-  for (int o = 1; o < 8; o <<= 1) {
-    r0.ss += __shfl_xor_sync(0xffffffffu, r0.ss, o);
-    r1.ss += __shfl_xor_sync(0xffffffffu, r1.ss, o);
+  const uint32_t row_bytes = (uint32_t)heads * kRowBytes;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < tokens_per_cta; ++i) mbar_init(&row_full[i], 1);
+    fence_mbar_init();
   }
-  finish_row(p, r0, gl);
-  finish_row(p, r1, gl);
+  __syncthreads();
+  const int64_t t = (int64_t)blockIdx.x * tokens_per_cta + warp;
+  if (warp >= tokens_per_cta || t >= p.num_tokens) return;
+  uint8_t *row = rows + (size_t)warp * row_bytes;
+  if (lane == 0) {
+    mbar_arrive_expect_tx(&row_full[warp], row_bytes);
+    bulk_copy_g2s(row, p.qkv + t * p.tok_stride, row_bytes, &row_full[warp]);
+  }
+  // while the row is in flight: this token's position, slot and cos/sin
+  const int64_t pos = p.positions[t];
+  const int64_t slot = p.slots[t];
+  const bool pos_ok = pos >= 0 && pos < p.max_position;
+  const bool slot_ok = slot >= 0 && slot < p.num_slots;
+  if (lane == 0) {
+    if (!pos_ok) record_error(p.err, 32u /* POSITION_RANGE */);
+    if (slot >= p.num_slots) record_error(p.err, 1u /* SLOT_RANGE */);
+  }
+  float4 cs[4] = {};
+  if (pos_ok) {
+    const float4 *src = reinterpret_cast<const float4 *>(p.cos_sin + pos * kD);
+    cs[0] = src[2 * gl];
+    cs[1] = src[2 * gl + 1];
+    cs[2] = src[16 + 2 * gl];
+    cs[3] = src[16 + 2 * gl + 1];
+  }
+  if (!__all_sync(0xffffffffu, wait_parity(&row_full[warp], 0, p.err))) return;
+  if (pos_ok) {
+    // query and key heads, eight rows per pass (two per quarter warp); every lane takes part
+    // in the shuffles, rows past the key heads contribute zeros
+    const int nqk = p.hq + p.hkv;
+    for (int h0 = 0; h0 < nqk; h0 += 8) {
+      const int ha = h0 + group, hb = h0 + 4 + group;
+      uint8_t *ra = row + (size_t)ha * kRowBytes, *rb = row + (size_t)hb * kRowBytes;
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      const uint4 alo = ha < nqk ? reinterpret_cast<const uint4 *>(ra)[gl] : z;
+      const uint4 ahi = ha < nqk ? reinterpret_cast<const uint4 *>(ra + kHalf * 2)[gl] : z;
+      const uint4 blo = hb < nqk ? reinterpret_cast<const uint4 *>(rb)[gl] : z;
+      const uint4 bhi = hb < nqk ? reinterpret_cast<const uint4 *>(rb + kHalf * 2)[gl] : z;
+      float sa = sum_sq(alo, ahi), sb = sum_sq(blo, bhi);
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) {
+        sa += __shfl_xor_sync(0xffffffffu, sa, o);
+        sb += __shfl_xor_sync(0xffffffffu, sb, o);
+      }
+      if (ha < nqk) finish_row(p, ra, alo, ahi, sa, ha < p.hq, cs, gl);
+      if (hb < nqk) finish_row(p, rb, blo, bhi, sb, hb < p.hq, cs, gl);
+    }
+    fence_async_shared();  // the rows written above are read by the bulk copies below
+  }
+  __syncwarp();
+  if (lane == 0) {
+    const uint32_t q_bytes = (uint32_t)p.hq * kRowBytes, kv_bytes = (uint32_t)p.hkv * kRowBytes;
+    if (pos_ok) bulk_copy_s2g(p.q_out + t * p.hq * kD, row, q_bytes);
+    if (slot_ok) {
+      if (pos_ok) bulk_copy_s2g(p.k_cache + slot * p.hkv * kD, row + q_bytes, kv_bytes);
+      bulk_copy_s2g(p.v_cache + slot * p.hkv * kD, row + q_bytes + kv_bytes, kv_bytes);
+    }
+    bulk_commit();
+    bulk_wait_read_all();  // the row must stay in shared memory until the copies have read it
+  }
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -222,11 +231,17 @@ extern "C" pkv_status pkv_qk_norm_rope_store(
     return PKV_ERR_UNSUPPORTED;
   unsigned int *err = current_error_word();
   if (!err) return PKV_ERR_CUDA;
-  const int64_t rows_per_warp = kRowsPerQuarter * kRowsPerWarp;
-  const int64_t warps_per_token = (num_q_heads + 2 * num_kv_heads + rows_per_warp - 1) / rows_per_warp;
-  const int64_t warps = num_tokens * warps_per_token;
-  const int64_t grid = (warps + kThreads / 32 - 1) / (kThreads / 32);
-  if (grid * (kThreads / 32) > UINT32_MAX || grid > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  const int64_t row_bytes = (int64_t)(num_q_heads + 2 * num_kv_heads) * head_dim * 2;
+  const int64_t tpc = row_bytes > kMaxSmem ? 1 : std::min<int64_t>(kMaxTokensPerCta, kMaxSmem / row_bytes);
+  const int64_t smem = tpc * row_bytes;
+  if (smem > 227 * 1024) return PKV_ERR_UNSUPPORTED;
+  const int64_t grid = (num_tokens + tpc - 1) / tpc;
+  if (grid > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  if (smem > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        qk_norm_rope_store_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return PKV_ERR_CUDA;
+  }
   RopeParams prm{};
   prm.qkv = static_cast<const uint16_t *>(qkv);
   prm.tok_stride = qkv_tok_stride;
@@ -245,7 +260,7 @@ extern "C" pkv_status pkv_qk_norm_rope_store(
   prm.hq = num_q_heads;
   prm.hkv = num_kv_heads;
   prm.err = err;
-  qk_norm_rope_store_kernel<<<(unsigned)grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-      prm, (uint32_t)warps_per_token);
+  qk_norm_rope_store_kernel<<<(unsigned)grid, (unsigned)(tpc * 32), (size_t)smem,
+                              static_cast<cudaStream_t>(stream)>>>(prm, (int)tpc);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

@@ -35,9 +35,6 @@ __device__ __forceinline__ void tc_fence_after_sync() {
 }
 
 // Make this thread's generic-proxy shared-memory writes visible to the async proxy (UMMA).
-__device__ __forceinline__ void fence_async_shared() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 
 // ------------------------------------------------------------------ UMMA
 // D[tmem] (+)= A[smem desc] * B[smem desc], kind::f16 (bf16 in, fp32 accumulate), 1 CTA.
