@@ -8,6 +8,8 @@
 // rows stay in L2 for the attention kernel that reads them next.
 //
 // HBM traffic per token: 2 rows read + 2 rows written + 8 bytes of slot (algorithmic minimum).
+#include <algorithm>
+
 #include "device_common.cuh"
 #include "launch.h"
 
@@ -46,6 +48,40 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
       v_cache[slot * kRow + i * 32 + lane] = vr[i];
     }
   }
+}
+
+// Rows staged through shared memory with 1-D bulk copies: lane i of a CTA moves token
+// blockIdx.x * tokens_per_cta + i (its K row and V row in, both out to the slot's pool rows),
+// so a CTA keeps up to 8 tokens in flight and the copies run on the TMA engine.
+constexpr int kBulkTokensPerCta = 8;
+__global__ void __launch_bounds__(32)
+    kv_store_bulk_kernel(const uint8_t *__restrict__ k, int64_t k_stride, const uint8_t *__restrict__ v,
+                         int64_t v_stride, const int64_t *__restrict__ slot_mapping,
+                         int64_t num_tokens, uint8_t *__restrict__ k_cache,
+                         uint8_t *__restrict__ v_cache, int64_t num_slots, uint32_t row_bytes,
+                         int tokens_per_cta, unsigned int *err) {
+  extern __shared__ __align__(128) uint8_t buf[];  // tokens_per_cta x (K row, V row)
+  __shared__ uint64_t full[kBulkTokensPerCta];
+  const int i = threadIdx.x;
+  const int64_t t = (int64_t)blockIdx.x * tokens_per_cta + i;
+  if (i >= tokens_per_cta || t >= num_tokens) return;
+  const int64_t slot = __ldg(slot_mapping + t);
+  if (slot < 0) return;
+  if (slot >= num_slots) {
+    record_error(err, 1u /* PKV_DEVERR_SLOT_RANGE */);
+    return;
+  }
+  uint8_t *kb = buf + (size_t)i * 2 * row_bytes, *vb = kb + row_bytes;
+  mbar_init(&full[i], 1);  // this thread's own barrier: no other thread touches it
+  fence_mbar_init();
+  mbar_arrive_expect_tx(&full[i], 2 * row_bytes);
+  bulk_copy_g2s(kb, k + t * k_stride, row_bytes, &full[i]);
+  bulk_copy_g2s(vb, v + t * v_stride, row_bytes, &full[i]);
+  if (!wait_parity(&full[i], 0, err)) return;
+  bulk_copy_s2g(k_cache + slot * row_bytes, kb, row_bytes);
+  bulk_copy_s2g(v_cache + slot * row_bytes, vb, row_bytes);
+  bulk_commit();
+  bulk_wait_read_all();  // the rows must stay in shared memory until the copies have read them
 }
 
 // Any row length that is a whole number of 16-byte vectors.
@@ -111,7 +147,26 @@ cudaError_t launch_kv_store(const void *k, int64_t k_tok_stride, const void *v,
   auto aligned16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
   const bool vec_ok = (row_elems % 8 == 0) && (k_tok_stride % 8 == 0) && (v_tok_stride % 8 == 0) &&
                       aligned16(k) && aligned16(v) && aligned16(k_cache) && aligned16(v_cache);
-  if (vec_ok) {
+  const int64_t row_bytes = row_elems * 2;
+  const int64_t bulk_tpc = row_bytes > 0 ? std::min<int64_t>(kBulkTokensPerCta, (96 * 1024) / (2 * row_bytes)) : 0;
+  if (vec_ok && bulk_tpc >= 1) {
+    const int64_t smem = bulk_tpc * 2 * row_bytes;
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (smem > 48 * 1024 && (dev >= 64 || !configured[dev])) {
+      const cudaError_t e = cudaFuncSetAttribute(
+          kv_store_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+      if (e != cudaSuccess) return e;
+      if (dev < 64) configured[dev] = true;
+    }
+    const int64_t grid = (num_tokens + bulk_tpc - 1) / bulk_tpc;
+    if (grid > INT32_MAX) return cudaErrorInvalidValue;
+    kv_store_bulk_kernel<<<(unsigned)grid, 32, (size_t)smem, stream>>>(
+        static_cast<const uint8_t *>(k), k_tok_stride * 2, static_cast<const uint8_t *>(v),
+        v_tok_stride * 2, slot_mapping, num_tokens, static_cast<uint8_t *>(k_cache),
+        static_cast<uint8_t *>(v_cache), num_slots, (uint32_t)row_bytes, (int)bulk_tpc, err);
+  } else if (vec_ok) {
     const int64_t row_v = row_elems / 8;
     const uint4 *k4 = static_cast<const uint4 *>(k);
     const uint4 *v4 = static_cast<const uint4 *>(v);
