@@ -1,11 +1,10 @@
 // kv_store.cu -- scatter each new token's K and V rows into the paged pool via slot_mapping.
 //
 // The store of «nano-vLLM 最小化vLLM重新实现», 架构 5 (store_kvcache: K/V written into the
-// paged cache through slot_mapping). One warp moves one token: its K row and its V row
-// (num_kv_heads * head_dim bf16 each; 2 KiB for Qwen3's 8 x 128), as 16-byte vectors, so a
-// warp instruction moves 512 contiguous bytes. All of a lane's loads are issued before its
-// stores. Loads bypass L1 (each byte is read once); stores are ordinary write-back so the
-// rows stay in L2 for the attention kernel that reads them next.
+// paged cache through slot_mapping). Rows that are whole 16-byte multiples go through shared
+// memory with 1-D bulk copies (one thread per token: K and V rows in, then out to the slot's
+// pool rows), which keeps many tokens in flight on the TMA engine with no registers held.
+// Longer rows use 16-byte vectors, one warp per token; unaligned rows go 2 bytes at a time.
 //
 // HBM traffic per token: 2 rows read + 2 rows written + 8 bytes of slot (algorithmic minimum).
 #include <algorithm>
@@ -17,38 +16,6 @@ namespace pkv {
 namespace {
 
 constexpr int kWarpsPerCta = 8;
-
-// Rows of exactly VEC 16-byte vectors per lane (row = 32 * VEC vectors): fully unrolled.
-template <int VEC>
-__global__ void __launch_bounds__(kWarpsPerCta * 32)
-    kv_store_rows_kernel(const uint4 *__restrict__ k, int64_t k_stride, const uint4 *__restrict__ v,
-                         int64_t v_stride, const int64_t *__restrict__ slot_mapping,
-                         int64_t num_tokens, uint4 *__restrict__ k_cache,
-                         uint4 *__restrict__ v_cache, int64_t num_slots, unsigned int *err) {
-  const int lane = threadIdx.x & 31;
-  const int64_t warp0 = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
-  const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerCta;
-  constexpr int64_t kRow = 32 * VEC;  // vectors per row
-  for (int64_t t = warp0; t < num_tokens; t += nwarps) {
-    const int64_t slot = __ldg(slot_mapping + t);
-    uint4 kr[VEC], vr[VEC];
-#pragma unroll
-    for (int i = 0; i < VEC; ++i) {
-      kr[i] = ld_stream_u4(k + t * k_stride + i * 32 + lane);
-      vr[i] = ld_stream_u4(v + t * v_stride + i * 32 + lane);
-    }
-    if (slot < 0) continue;
-    if (slot >= num_slots) {
-      if (lane == 0) record_error(err, 1u /* PKV_DEVERR_SLOT_RANGE */);
-      continue;
-    }
-#pragma unroll
-    for (int i = 0; i < VEC; ++i) {
-      k_cache[slot * kRow + i * 32 + lane] = kr[i];
-      v_cache[slot * kRow + i * 32 + lane] = vr[i];
-    }
-  }
-}
 
 // Rows staged through shared memory with 1-D bulk copies: lane i of a CTA moves token
 // blockIdx.x * tokens_per_cta + i (its K row and V row in, both out to the slot's pool rows),
@@ -166,30 +133,11 @@ cudaError_t launch_kv_store(const void *k, int64_t k_tok_stride, const void *v,
         static_cast<const uint8_t *>(k), k_tok_stride * 2, static_cast<const uint8_t *>(v),
         v_tok_stride * 2, slot_mapping, num_tokens, static_cast<uint8_t *>(k_cache),
         static_cast<uint8_t *>(v_cache), num_slots, (uint32_t)row_bytes, (int)bulk_tpc, err);
-  } else if (vec_ok) {
-    const int64_t row_v = row_elems / 8;
-    const uint4 *k4 = static_cast<const uint4 *>(k);
-    const uint4 *v4 = static_cast<const uint4 *>(v);
-    uint4 *kc4 = static_cast<uint4 *>(k_cache);
-    uint4 *vc4 = static_cast<uint4 *>(v_cache);
-    const int64_t ks = k_tok_stride / 8, vs = v_tok_stride / 8;
-    switch (row_v) {
-      case 128:  // 8 heads x 128 dims: the Qwen3 row
-        kv_store_rows_kernel<4><<<ctas, block, 0, stream>>>(k4, ks, v4, vs, slot_mapping,
-                                                            num_tokens, kc4, vc4, num_slots, err);
-        break;
-      case 64:
-        kv_store_rows_kernel<2><<<ctas, block, 0, stream>>>(k4, ks, v4, vs, slot_mapping,
-                                                            num_tokens, kc4, vc4, num_slots, err);
-        break;
-      case 256:
-        kv_store_rows_kernel<8><<<ctas, block, 0, stream>>>(k4, ks, v4, vs, slot_mapping,
-                                                            num_tokens, kc4, vc4, num_slots, err);
-        break;
-      default:
-        kv_store_vec_kernel<<<ctas, block, 0, stream>>>(k4, ks, v4, vs, slot_mapping, num_tokens,
-                                                        kc4, vc4, num_slots, row_v, err);
-    }
+  } else if (vec_ok) {  // rows too long to stage: 16-byte vectors straight through
+    kv_store_vec_kernel<<<ctas, block, 0, stream>>>(
+        static_cast<const uint4 *>(k), k_tok_stride / 8, static_cast<const uint4 *>(v),
+        v_tok_stride / 8, slot_mapping, num_tokens, static_cast<uint4 *>(k_cache),
+        static_cast<uint4 *>(v_cache), num_slots, row_elems / 8, err);
   } else {
     kv_store_u16_kernel<<<ctas, block, 0, stream>>>(
         static_cast<const uint16_t *>(k), k_tok_stride, static_cast<const uint16_t *>(v),
