@@ -80,8 +80,10 @@ def _check(full, qkv, qw, kw, table, pos, slots, nb, hq, hkv, q, kc, vc, what):
 
 
 @pytest.mark.parametrize("T,hq,hkv", [(1, 16, 8), (5, 16, 8), (257, 16, 8), (64, 8, 8),
-                                      (33, 32, 4)])
+                                      (33, 32, 4), (11, 96, 16), (3, 400, 8)])
 def test_qk_norm_rope_store_matches_oracle(T, hq, hkv):
+    """Eight tokens per CTA for the usual head counts; 128 heads (32 KiB rows) stage three
+    tokens per CTA, and 416 heads (104 KiB rows) one."""
     c = _case(T, hq, hkv, seed=T + hq)
     q, kc, vc = _run_gpu(*c, hq, hkv)
     _check(*c, hq, hkv, q, kc, vc, f"T={T} hq={hq} hkv={hkv}")

@@ -44,12 +44,14 @@ def test_store_tiny_decode_step():
 
 
 @pytest.mark.parametrize("hkv,d,bs", [(8, 128, 16), (4, 128, 16), (16, 128, 16), (2, 64, 16),
-                                      (3, 40, 16), (3, 4, 16), (200, 128, 2)])
+                                      (3, 40, 16), (3, 4, 16), (64, 128, 4), (200, 128, 2)])
 def test_store_row_shapes(hkv, d, bs):
-    """Bulk copies through shared memory for rows that are whole 16-byte vectors (any count);
+    """Bulk copies through shared memory for rows that are whole 16-byte vectors (any count;
+    16 KiB rows stage three tokens per CTA instead of eight);
     16-byte vectors straight through for rows too long to stage (200 x 128 bf16 = 50 KiB); a
     2-byte path for rows that are not whole vectors (3 x 4 bf16 = 24 bytes)."""
     k, v, slots, kc = _store_case(77, 6 if bs == 16 else 48, bs, hkv, d, 5, neg=(3, 40))
+    assert len(slots) <= kc.shape[0] * kc.shape[1]
     kc_o, vc_o, kc_g, vc_g = _run_both(k, v, slots, kc)
     assert np.array_equal(kc_g, kc_o) and np.array_equal(vc_g, vc_o)
 
