@@ -96,6 +96,52 @@ def test_prefill_argument_checks():
     assert _prefill(wsb=need - 16) == pkv.ERR_WORKSPACE            # the work list does not fit
 
 
+def _step(**kw):
+    a = dict(q=FAKE, kn=FAKE, kns=1024, vn=FAKE, vns=1024, slots=FAKE, kc=FAKE, vc=FAKE, bt=FAKE,
+             W=4, cl=FAKE, B=2, maxc=100, hq=16, hkv=8, d=128, bs=256, nb=10, scale=0.088, ns=0,
+             ws=FAKE, wsb=1 << 20, out=FAKE)
+    a.update(kw)
+    return L.pkv_paged_decode_step(a["q"], a["kn"], a["kns"], a["vn"], a["vns"], a["slots"],
+                                   a["kc"], a["vc"], a["bt"], a["W"], a["cl"], a["B"], a["maxc"],
+                                   a["hq"], a["hkv"], a["d"], a["bs"], a["nb"], a["scale"],
+                                   a["ns"], a["ws"], a["wsb"], a["out"], None)
+
+
+def test_decode_step_argument_checks():
+    assert _step(B=0) == pkv.OK
+    assert _step(B=-1) == pkv.ERR_INVALID_ARG
+    assert _step(kns=512) == pkv.ERR_INVALID_ARG                   # new K rows shorter than Hkv*D
+    assert _step(slots=None) == pkv.ERR_INVALID_ARG
+    assert _step(hq=12, hkv=8) == pkv.ERR_INVALID_ARG
+    assert _step(scale=float("inf")) == pkv.ERR_INVALID_ARG
+    assert _step(d=64, kns=512, vns=512) == pkv.ERR_UNSUPPORTED
+    assert _step(bs=128) == pkv.ERR_UNSUPPORTED
+    assert _step(kns=1028) == pkv.ERR_UNSUPPORTED                  # stride not a 16-byte multiple
+    assert _step(vn=ctypes.c_void_p(0x1008)) == pkv.ERR_UNSUPPORTED  # not 16-byte aligned
+
+
+def _rope(**kw):
+    a = dict(qkv=FAKE, ts=4096, T=4, pos=FAKE, qw=FAKE, kw=FAKE, eps=1e-6, cs=FAKE, maxp=1024,
+             slots=FAKE, q=FAKE, kc=FAKE, vc=FAKE, nslots=512, hq=16, hkv=8, d=128)
+    a.update(kw)
+    return L.pkv_qk_norm_rope_store(a["qkv"], a["ts"], a["T"], a["pos"], a["qw"], a["kw"],
+                                    a["eps"], a["cs"], a["maxp"], a["slots"], a["q"], a["kc"],
+                                    a["vc"], a["nslots"], a["hq"], a["hkv"], a["d"], None)
+
+
+def test_qk_norm_rope_store_argument_checks():
+    assert _rope(T=0) == pkv.OK
+    assert _rope(T=-1) == pkv.ERR_INVALID_ARG
+    assert _rope(ts=4000) == pkv.ERR_INVALID_ARG                   # shorter than a projection row
+    assert _rope(eps=float("nan")) == pkv.ERR_INVALID_ARG
+    assert _rope(eps=-1.0) == pkv.ERR_INVALID_ARG
+    assert _rope(maxp=0) == pkv.ERR_INVALID_ARG
+    assert _rope(pos=None) == pkv.ERR_INVALID_ARG
+    assert _rope(d=64, ts=2048) == pkv.ERR_UNSUPPORTED
+    assert _rope(ts=4100) == pkv.ERR_UNSUPPORTED                   # stride not a 16-byte multiple
+    assert _rope(q=ctypes.c_void_p(0x1008)) == pkv.ERR_UNSUPPORTED  # not 16-byte aligned
+
+
 def test_workspace_query_without_device_is_zero_or_sized():
     n = L.pkv_decode_workspace_bytes(4, 16, 8, 128, 300, 0)
     assert n == 0 or n >= 16   # 0 without a device to plan for
