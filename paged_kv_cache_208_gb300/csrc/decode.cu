@@ -136,6 +136,9 @@ __global__ void __maxnreg__(96)
     fence_mbar_init();
   }
   if (__syncthreads_or(threadIdx.x == 0 && aborted(p.err))) return;  // uniform across the CTA
+  // the merge kernel that follows may be scheduled now: it waits for this grid's completion
+  // (and its memory) before reading anything
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------------ producer
@@ -486,6 +489,9 @@ __global__ void __launch_bounds__(128)
                           const int32_t *__restrict__ context_lens, int32_t batch,
                           int32_t num_q_heads, int32_t chunk, int32_t splits, int64_t cap,
                           uint16_t *__restrict__ out) {
+  // launched as a programmatic dependent of the split kernel: wait until that grid has
+  // completed and its partial results are visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
   if (row >= (int64_t)batch * num_q_heads) return;
   const int lane = threadIdx.x & 31;
@@ -648,10 +654,20 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &p, cudaSt
                            : launch_split<1>(km, vm, prm, a.num_sms, stream);
   if (e != cudaSuccess || p.splits == 1) return e;
   const int64_t rows_out = (int64_t)a.batch * a.num_q_heads;
-  decode_combine_kernel<<<(unsigned)((rows_out + 3) / 4), 128, 0, stream>>>(
-      prm.part_o, prm.part_lse, a.context_lens, a.batch, a.num_q_heads, p.chunk, p.splits,
-      prm.cap, static_cast<uint16_t *>(a.out));
-  return cudaGetLastError();
+  // programmatic dependent launch: the merge grid is set up while the split kernel runs
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)((rows_out + 3) / 4));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_combine_kernel, (const float *)prm.part_o,
+                            (const float *)prm.part_lse, a.context_lens, a.batch, a.num_q_heads,
+                            p.chunk, p.splits, prm.cap, static_cast<uint16_t *>(a.out));
 }
 
 }  // namespace pkv
