@@ -44,7 +44,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one decode_split_kernel launch on
 # the Qwen3 decode batch, from one ncu capture of the current kernel; None whenever the kernel
 # has changed since that capture.
-DECODE_SPLIT_DRAM_BYTES = 1_184_816_296
+DECODE_SPLIT_DRAM_BYTES = 1_184_348_160
 FALLBACK_BF16_TFLOPS = 1900.0
 WORKLOAD = ("qwen3-0.6b decode step: 28 layers x (kv_store of 256 new tokens + paged decode "
             "attention), B=256, ctx U[100,2048] (seed 2), block_size 256, 16 q / 8 kv heads, "
