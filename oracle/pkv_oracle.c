@@ -53,12 +53,15 @@ static double bf16_value(uint16_t bits)
     return (double)f;
 }
 
-static void set_threads(int32_t num_threads)
+/* Threads for one call: num_threads if positive, else every thread OpenMP offers. Passed to
+ * each parallel region, so one call's choice does not carry over to the next call. */
+static int threads_for(int32_t num_threads)
 {
 #ifdef _OPENMP
-    if (num_threads > 0) omp_set_num_threads(num_threads);
+    return num_threads > 0 ? num_threads : omp_get_max_threads();
 #else
     (void)num_threads;
+    return 1;
 #endif
 }
 
@@ -156,8 +159,9 @@ int32_t pkv_oracle_paged_decode(const uint16_t *q, const uint16_t *k_cache,
         return ORACLE_BAD_ARG;
     const int32_t group = num_q_heads / num_kv_heads;
     int32_t status = ORACLE_OK;
-    set_threads(num_threads);
-#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    const int nthreads = threads_for(num_threads);
+    (void)nthreads;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1) num_threads(nthreads)
     for (int32_t b = 0; b < B; ++b) {
         for (int32_t hq = 0; hq < num_q_heads; ++hq) {
             const int32_t h = hq / group;
@@ -210,8 +214,9 @@ int32_t pkv_oracle_varlen_prefill(const uint16_t *q, int64_t q_tok_stride, const
         return ORACLE_BAD_ARG;
     const int32_t group = num_q_heads / num_kv_heads;
     int32_t status = ORACLE_OK;
-    set_threads(num_threads);
-#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    const int nthreads = threads_for(num_threads);
+    (void)nthreads;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1) num_threads(nthreads)
     for (int32_t n = 0; n < N; ++n) {
         for (int32_t hq = 0; hq < num_q_heads; ++hq) {
             const int32_t h = hq / group;
