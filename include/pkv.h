@@ -96,8 +96,9 @@ pkv_status pkv_get_device_errors(uint32_t *errors, int32_t reset);
  * k_cache, v_cache: [num_slots, num_kv_heads, head_dim] bf16 (a per-layer pool,
  *                num_slots = num_blocks * block_size).
  * Returns PKV_ERR_INVALID_ARG for null pointers with num_tokens > 0, negative sizes, or
- * strides shorter than a row. Any head count and head_dim are accepted; rows whose byte
- * length and addresses are multiples of 16 take the vectorised path.
+ * strides shorter than a row. Any head count and head_dim are accepted: rows whose byte
+ * length, strides and addresses are multiples of 16 bytes move with bulk copies through
+ * shared memory (16-byte vectors for rows over 48 KiB), other rows two bytes at a time.
  */
 pkv_status pkv_kv_store(const void *k, int64_t k_tok_stride, const void *v, int64_t v_tok_stride,
                         const int64_t *slot_mapping, int64_t num_tokens, void *k_cache,
@@ -302,7 +303,8 @@ pkv_status pkv_paged_decode_attn_noalloc(const void *q, const void *k_cache, con
  * as pkv_kv_store writes them (negative slot: nothing stored, q still written; slot >=
  * num_slots: skipped and PKV_DEVERR_SLOT_RANGE). A position outside [0, max_position) skips the
  * token's query and key heads and sets PKV_DEVERR_POSITION_RANGE.
- * Implemented: head_dim == 128, 16-byte aligned pointers. Asynchronous on `stream`.
+ * Implemented: head_dim == 128, 16-byte aligned pointers, projection rows of at most 227 KiB
+ * (one token's row is staged in shared memory). Asynchronous on `stream`.
  */
 pkv_status pkv_qk_norm_rope_store(const void *qkv, int64_t qkv_tok_stride, int64_t num_tokens,
                                   const int64_t *positions, const void *q_norm_weight,
