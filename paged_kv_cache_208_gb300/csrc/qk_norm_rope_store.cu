@@ -234,14 +234,27 @@ extern "C" pkv_status pkv_qk_norm_rope_store(
   const int64_t row_bytes = (int64_t)(num_q_heads + 2 * num_kv_heads) * head_dim * 2;
   const int64_t tpc = row_bytes > kMaxSmem ? 1 : std::min<int64_t>(kMaxTokensPerCta, kMaxSmem / row_bytes);
   const int64_t smem = tpc * row_bytes;
-  if (smem > 227 * 1024) return PKV_ERR_UNSUPPORTED;
   const int64_t grid = (num_tokens + tpc - 1) / tpc;
   if (grid > INT32_MAX) return PKV_ERR_UNSUPPORTED;
-  if (smem > 48 * 1024) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        qk_norm_rope_store_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return PKV_ERR_CUDA;
+  // once per device: allow dynamic shared memory up to the per-CTA maximum
+  static int max_dynamic[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+  int limit = dev < 64 ? max_dynamic[dev] : 0;
+  if (limit == 0) {
+    int optin = 0;
+    cudaFuncAttributes fa{};
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess ||
+        cudaFuncGetAttributes(&fa, qk_norm_rope_store_kernel) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    limit = optin - (int)fa.sharedSizeBytes;
+    if (cudaFuncSetAttribute(qk_norm_rope_store_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, limit) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    if (dev < 64) max_dynamic[dev] = limit;
   }
+  if (smem > limit) return PKV_ERR_UNSUPPORTED;  // one token's row does not fit
   RopeParams prm{};
   prm.qkv = static_cast<const uint16_t *>(qkv);
   prm.tok_stride = qkv_tok_stride;
