@@ -3,7 +3,9 @@
 Every mutant is one textual change to a copy of ``oracle/pkv_oracle.c``, compiled with gcc
 into a temporary library; the shipped oracle source is never touched. A mutant survives if
 every pin in ``oracle_pins`` still passes, which would mean the pins cannot tell that mistake
-from the right answer. None of the mutants reads or writes out of bounds.
+from the right answer. None of the mutants reads or writes out of bounds. The block manager
+oracle (``oracle/block_manager.py``, plain Python) gets the same treatment against the pins in
+``block_manager_pins``, each mutant loaded from a temporary copy.
 """
 import os
 import shutil
@@ -94,3 +96,60 @@ def test_unmutated_copy_passes(tmp_path):
     L = oracle.load(obuild.build(str(path), str(tmp_path / "libcopy.so"), force=True))
     for pin in oracle_pins.ALL_PINS:
         oracle_pins.run_pin(pin, L)
+
+
+# ------------------------------------------------------------- the block manager oracle
+# Plausible mistakes in oracle/block_manager.py, each of which must fail at least one of its
+# pins (tests/block_manager_pins.py).
+BM_MUTANTS = [
+    ("xxh64_prime_typo", "0xC2B2AE3D27D4EB4F", "0xC2B2AE3D27D4EB4E", None),
+    ("xxh64_tail4_wrong_prime", 'h ^= (int.from_bytes(data[i:i + 4], "little") * P1) & M64',
+     'h ^= (int.from_bytes(data[i:i + 4], "little") * P2) & M64', None),
+    ("xxh64_no_avalanche_shift", "h ^= h >> 33", "h ^= h >> 0", None),
+    ("xxh64_length_not_added", "h = (h + n) & M64", "h = h & M64", None),
+    ("hash_not_chained", 'data = b"" if prefix is None else prefix.to_bytes(8, "little")',
+     'data = b""', None),
+    ("hash_tokens_8_bytes", '(t & 0xFFFFFFFF).to_bytes(4, "little")',
+     '(t & 0xFFFFFFFF).to_bytes(8, "little")', None),
+    ("free_list_lifo", "b = self.free.pop(0)", "b = self.free.pop()", None),
+    ("hit_without_token_check", "if b is not None and self.tokens[b] == toks:",
+     "if b is not None:", None),
+    ("dealloc_first_block_first", "for b in reversed(table):", "for b in table:", None),
+    ("no_upfront_block_check", "if len(self.free) < len(blocks):", "if False:", None),
+    ("append_hashes_wrong_block", "if n % bs == 0:", "if n % bs == 1:", None),
+    ("cached_blocks_not_counted", "cached += bs", "cached += 0", None),
+]
+
+
+def _load_module(path, name):
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(name, path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+@pytest.mark.parametrize("name,old,new,occ", BM_MUTANTS, ids=[m[0] for m in BM_MUTANTS])
+def test_block_manager_mutant_is_caught(tmp_path, name, old, new, occ):
+    import block_manager_pins
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "block_manager.py")).read()
+    path = tmp_path / f"bm_{name}.py"
+    path.write_text(_mutate(src, old, new, occ))
+    mod = _load_module(str(path), f"bm_mutant_{name}")
+    failures = []
+    for pin in block_manager_pins.ALL_PINS:
+        try:
+            pin(mod)
+        except Exception:  # an assertion, or the mutant crashing on the pin's inputs
+            failures.append(pin.__name__)
+    assert failures, f"block manager mutant {name} survives every pin"
+
+
+def test_block_manager_unmutated_copy_passes(tmp_path):
+    import block_manager_pins
+    src = os.path.join(os.path.dirname(oracle.__file__), "block_manager.py")
+    path = tmp_path / "bm_copy.py"
+    shutil.copy(src, path)
+    mod = _load_module(str(path), "bm_copy")
+    for pin in block_manager_pins.ALL_PINS:
+        pin(mod)
