@@ -287,3 +287,34 @@ def test_prefix_prefill_full_size():
     for n, ref in zip(seqs, refs):
         assert_attention_close(out[int(cq[n]):int(cq[n + 1])], ref, f"seq {n}")
     assert pkv.get_device_errors() == 0
+
+
+def test_prefill_one_32k_prompt_sampled_rows():
+    """One causal prompt of 32768 tokens (256 query blocks of 128, the longest rows read 256 key
+    tiles); sampled query rows checked against the oracle, each as a one-query sequence over
+    the keys up to its position (the bottom-right alignment makes that query see exactly
+    keys 0 .. p)."""
+    L = 32768
+    q_d = w.device_bf16_normal((L, 16, 128), 611)
+    k_d = w.device_bf16_normal((L, 8, 128), 612)
+    v_d = w.device_bf16_normal((L, 8, 128), 613)
+    cq = np.array([0, L], np.int32)
+    out = pkv.varlen_prefill_attn(q_d, k_d, v_d, dev(cq), dev(cq), L, L, 128 ** -0.5)
+    for p in (0, 1, 127, 128, 4095, 16384, 30000, L - 1):
+        qn = host_bits(q_d[p:p + 1])
+        kn, vn = host_bits(k_d[:p + 1]), host_bits(v_d[:p + 1])
+        ref = oracle.varlen_prefill(qn, kn, vn, np.array([0, 1], np.int32),
+                                    np.array([0, p + 1], np.int32), 128 ** -0.5)
+        assert_attention_close(out[p:p + 1], ref, f"row {p}")
+    assert pkv.get_device_errors() == 0
+
+
+def test_prefill_three_thousand_tiny_prompts():
+    """3000 prompts of 1 .. 40 tokens: the planning kernel's count, rank and fill loops take
+    several passes over its 1024 threads; every row checked against the oracle."""
+    g = w.rng(620)
+    lens = g.integers(1, 41, 3000)
+    q, k, v, cq, ck = _case(lens, seed=621)
+    ref = oracle.varlen_prefill(q, k, v, cq, ck, 128 ** -0.5)
+    assert_attention_close(_run(q, k, v, cq, ck), ref, "3000 tiny prompts")
+    assert pkv.get_device_errors() == 0
