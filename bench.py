@@ -413,10 +413,10 @@ def time_qk_norm_rope_store(pkv, hbm_peak: float, iters: int = 20):
             "l2": "inputs (2.4 GB) larger than L2"}
 
 
-def time_prefill(pkv, iters: int = 10):
+def time_prefill(pkv, iters: int = 10, lens=None):
     """Varlen causal prefill attention: 256 prompts, lengths U[100, 1024], packed layout;
-    one layer timed (x28 for a model)."""
-    lens = w.varlen_prefill_lengths()
+    one layer timed (x28 for a model). `lens` replaces the prompt lengths."""
+    lens = w.varlen_prefill_lengths() if lens is None else np.asarray(lens, np.int32)
     cu = torch.from_numpy(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)).cuda()
     T = int(lens.sum())
     q = w.device_bf16_normal((T, HQ, D), 401)
@@ -551,6 +551,13 @@ def run_ours(args):
         if "tflops" in extra["prefill"]:
             extra["prefill"]["frac_of_bf16_peak"] = extra["prefill"]["tflops"] / bf16_peak
             extra["prefill"]["tflops_x28_layers_ms"] = extra["prefill"]["ms"] * LAYERS
+        # the same kernel on long prompts (16 x 8192 tokens): few item switches and diagonal
+        # tiles, so this is its steady-state rate, beside the short prompts above
+        extra["prefill_long_prompts"] = time_prefill(pkv, iters=5, lens=[8192] * 16)
+        if "tflops" in extra["prefill_long_prompts"]:
+            extra["prefill_long_prompts"]["frac_of_bf16_peak"] = (
+                extra["prefill_long_prompts"]["tflops"] / bf16_peak)
+            extra["prefill_long_prompts"]["prompts"] = "16 x 8192 tokens, causal, packed"
         extra["prefix_prefill"] = time_prefix_prefill(pkv)
         extra["prefix_prefill"]["frac_of_bf16_peak"] = extra["prefix_prefill"]["tflops"] / bf16_peak
 
