@@ -41,11 +41,14 @@ B, HQ, HKV, D, BS = 256, w.NUM_Q_HEADS, w.NUM_KV_HEADS, w.HEAD_DIM, w.BLOCK_SIZE
 ROW_BYTES = HKV * D * 2                     # one token's K (or V) row in one layer
 BLOCK_BYTES_ALL_LAYERS = 2 * LAYERS * BS * ROW_BYTES
 FALLBACK_HBM_GBS = 6800.0
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one decode_split_kernel launch on
-# the Qwen3 decode batch, from one ncu capture of the current kernel; None whenever the kernel
-# has changed since that capture.
-DECODE_SPLIT_DRAM_BYTES = 1_184_348_160
 FALLBACK_BF16_TFLOPS = 1900.0
+# The committed ncu summary of decode_split_kernel on the Qwen3 decode batch. It records the
+# DRAM bytes of one launch and a hash of the kernel's sources at the time of the capture; the
+# bench reports that traffic only while the sources still hash the same.
+DECODE_PROFILE = os.path.join(ROOT, "profiles", "decode_split_qwen3_decode_batch.md")
+DECODE_SOURCES = ("paged_kv_cache_208_gb300/csrc/decode.cu",
+                  "paged_kv_cache_208_gb300/csrc/device_common.cuh")
+MIN_TIMED_SECONDS = 2.0   # the headline's K-step blocks are repeated until they cover this
 WORKLOAD = ("qwen3-0.6b decode step: 28 layers x (kv_store of 256 new tokens + paged decode "
             "attention), B=256, ctx U[100,2048] (seed 2), block_size 256, 16 q / 8 kv heads, "
             "head_dim 128, bf16 N(0,1), pool [2,28,NB,256,8,128] at 90% of free HBM")
@@ -117,6 +120,37 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def sources_sha256(paths) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in paths:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def decode_traffic():
+    """(DRAM bytes per launch, note) from the committed decode profile: the bytes are None
+    when the profile is missing or the kernel's sources changed after the capture."""
+    fields = {}
+    try:
+        with open(DECODE_PROFILE) as f:
+            for line in f:
+                if line.startswith("- ") and ": " in line:
+                    k, v = line[2:].split(": ", 1)
+                    fields[k.strip()] = v.strip().strip("`")
+    except OSError:
+        return None, "no committed profile"
+    try:
+        nbytes = int(fields["dram_bytes_per_launch"])
+        sha = fields["sources_sha256"]
+    except (KeyError, ValueError):
+        return None, "profile has no machine-readable traffic line"
+    if sha != sources_sha256(DECODE_SOURCES):
+        return None, "kernel sources changed since the ncu capture"
+    return nbytes, f"ncu capture in {os.path.relpath(DECODE_PROFILE, ROOT)} (sources {sha[:12]})"
 
 
 def dist_env():
@@ -506,23 +540,31 @@ def run_ours(args):
         raise RuntimeError("device error bits set during warm-up")
 
     with ClockSampler(torch.cuda.current_device()) as clocks:
-        # timed region 1: the headline, K steps back to back
-        barrier(world)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(args.steps):
-            step.run()
-        e1.record()
-        torch.cuda.synchronize()
-        barrier(world)
-        # timed region 2: the same K steps with an event pair around every decode call, for
-        # the decode kernel's own launch duration (roofline)
+        # timed region 1: the headline, blocks of exactly K steps back to back, each bracketed
+        # by a barrier and a synchronize; blocks repeat until they cover MIN_TIMED_SECONDS so
+        # that the clock sampler sees the GPU under load (value: the median block)
+        block_times, covered = [], 0.0
+        while covered < MIN_TIMED_SECONDS or not block_times:
+            barrier(world)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(args.steps):
+                step.run()
+            e1.record()
+            torch.cuda.synchronize()
+            barrier(world)
+            block_times.append(max_over_ranks(e0.elapsed_time(e1) / 1e3, world))
+            covered += block_times[-1]
+            if len(block_times) >= 1000:
+                break
+        # timed region 2: K steps with an event pair around every decode call, for the decode
+        # kernel's own launch duration (roofline)
         events = []
         for _ in range(args.steps):
             step.run(events)
         torch.cuda.synchronize()
-    elapsed = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+    elapsed = statistics.median(block_times)
     per_step = elapsed / args.steps
     decode_times = [a.elapsed_time(b) / 1e3 for a, b in zip(events[0::2], events[1::2])]
     decode_avg = sum(decode_times) / len(decode_times)
@@ -589,6 +631,7 @@ def run_ours(args):
         return
     total_bytes = step.step_bytes * world
     dec_bytes = step.bytes["decode"] + step.bytes["store"]  # the call stores and attends
+    traffic, traffic_note = decode_traffic()
     achieved = dec_bytes / decode_avg / 1e9
     line = {
         "metric": METRIC,
@@ -607,6 +650,7 @@ def run_ours(args):
                    "sum_ctx": int(step.lay.context_lens.sum()), "num_blocks": step.num_blocks,
                    "pool_gb": round(step.pool.numel() * 2 / 1e9, 1),
                    "splits": args.num_splits or "auto", "l2": "inputs larger than L2 (1.13 GB of KV per layer)",
+                   "timed_blocks": len(block_times), "timed_seconds": round(covered, 3),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "kv_tokens_per_s": step.kv_tokens * world / per_step,
         "decode_frac_of_hbm_peak": achieved / hbm_peak,
@@ -614,8 +658,9 @@ def run_ours(args):
                      "kernel": "paged_decode_step (split kernel with the store, + combine)",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "peak_source": peak_src,
-                     "traffic": DECODE_SPLIT_DRAM_BYTES,
+                     "traffic": traffic,
                      "traffic_kernel": "decode_split_kernel (ncu, one launch, same workload)",
+                     "traffic_source": traffic_note,
                      "algorithmic_bytes_per_launch": dec_bytes,
                      "avg_launch_us": decode_avg * 1e6},
         "e2e": {"value": total_bytes / e2e_dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
@@ -623,6 +668,7 @@ def run_ours(args):
                 "copies": "pinned host <-> device every step, on a second stream overlapping "
                           "the neighbouring steps' compute (two device buffer sets)"},
         "gpu_launches": step.launches_per_step() * args.steps,
+        "gpu_launches_counted_over": "one timed block of K steps",
         "clocks": clocks.summary(),
         "cpu_baseline": cpu,
         "extra": extra,
@@ -630,19 +676,39 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
 
 
+def reference_inputs(seqs: int = 16, seed: int = 2):
+    """Inputs of one layer of the decode step for the reference arm, made on the host alone:
+    the first `seqs` sequences of the Qwen3 decode batch (their lengths, block draws and new
+    tokens' slots), a compact pool of just the blocks they reference, and bf16 N(0,1) values
+    drawn with numpy. No device memory and no part of the CUDA library are involved."""
+    import oracle  # the reference arm times the oracle
+    ctx_all = w.qwen3_decode_lengths(seed)
+    lay = w.qwen3_decode_layout(w.blocks_needed(ctx_all) + 64, seed)
+    rows = np.arange(seqs)
+    tabs = lay.block_tables[rows]
+    ids = np.unique(tabs[tabs >= 0])
+    remap = np.full(lay.num_blocks, -1, np.int64)
+    remap[ids] = np.arange(len(ids))
+    bt = np.where(tabs >= 0, remap[np.maximum(tabs, 0)], -1).astype(np.int32)
+    slots = remap[lay.slot_mapping[rows] // BS] * BS + lay.slot_mapping[rows] % BS
+    g = w.rng(10_000 + seed)
+    return dict(oracle=oracle, q=w.host_bf16_normal(g, (seqs, HQ, D)),
+                kn=w.host_bf16_normal(g, (seqs, HKV, D)), vn=w.host_bf16_normal(g, (seqs, HKV, D)),
+                kc=w.host_bf16_normal(g, (len(ids), BS, HKV, D)),
+                vc=w.host_bf16_normal(g, (len(ids), BS, HKV, D)), bt=bt,
+                ctx=lay.context_lens[rows], slots=slots.astype(np.int64),
+                bytes=decode_bytes(lay.context_lens[rows], lay.block_tables.shape[1]))
+
+
 def run_reference(args):
     """The CPU oracle timed on the host cores, on the same workload and metric: each step is a
-    bounded sample (16 of the 256 sequences of one layer: store + paged decode)."""
+    bounded sample (16 of the 256 sequences of one layer: store + paged decode). Its inputs are
+    made on the host (reference_inputs): this arm loads no part of the CUDA library."""
     rank, world, local = dist_env()
     if rank != 0:
         return
-    torch.cuda.set_device(local)
-    pkv = load_pkv()
-    step = DecodeStep(pkv, num_blocks=w.blocks_needed(w.qwen3_decode_lengths()) + 64)
-    step.run()
-    torch.cuda.synchronize()
-    import oracle
-    s = oracle_decode_sample(step, 16)
+    s = reference_inputs(16)
+    oracle = s["oracle"]
     base_kc, base_vc = s["kc"].copy(), s["vc"].copy()
     times = []
     for i in range(args.warmup + args.steps):
@@ -654,12 +720,12 @@ def run_reference(args):
     nbytes = s["bytes"]["store"] + s["bytes"]["decode"]
     value = nbytes / per / 1e9
     sample = ("16 of the 256 sequences of one layer per step: kv_store + paged decode, "
-              "fp64 C oracle with OpenMP")
+              "fp64 C oracle with OpenMP, inputs drawn on the host")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (same seeded workload)",
+        "data": "synthetic (same seeded workload shape: lengths, block draws, slots)",
         "config": {"workload": WORKLOAD, "sample": sample},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.max_threads(),
                          "kind": "oracle", "sample": sample},

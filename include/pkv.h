@@ -267,6 +267,8 @@ pkv_status pkv_varlen_prefill_attn(const void *q, int64_t q_tok_stride, int64_t 
  *
  * The first call on each device looks up the array's device address (cudaGetSymbolAddress,
  * with that device current) and caches it; make that first call before any stream capture.
+ * A lookup that fails returns PKV_ERR_CUDA, is not cached (the next call tries again) and
+ * leaves no pending CUDA error behind.
  * All calls on a device share the array and it keeps the last call's contents (nothing needs
  * to start at zero). Calls whose kernels may run at the same time on the GPU (different
  * streams without ordering) race on the array: order them on one stream.

@@ -259,13 +259,14 @@ __global__ void __maxnreg__(96)
         tma_load_3d(sm.v[stage], &vmap, &sm.full[stage], 0, 2 * h, row, policy);
       }
     }
-    // keep the CTA alive until every copy it issued has landed
+    // keep the CTA alive until every copy it issued has landed (also after an abort: these
+    // waits ignore the abort bit; `tiles` and `pushed` count only issued copies)
     bool drained = true;
-    if (newkv_pending) drained = wait_parity(&sm.newkv_full[newkv_slot], (newkv_par >> newkv_slot) & 1, p.err);
+    if (newkv_pending) drained = wait_own(&sm.newkv_full[newkv_slot], (newkv_par >> newkv_slot) & 1, p.err);
     for (uint32_t t = tiles > kStages ? tiles - kStages : 0; drained && t < tiles; ++t)
-      drained = wait_parity(&sm.full[t % kStages], (t / kStages) & 1, p.err);
+      drained = wait_own(&sm.full[t % kStages], (t / kStages) & 1, p.err);
     for (uint32_t k = pushed > kRing ? pushed - kRing : 0; drained && k < pushed; ++k)
-      drained = wait_parity(&sm.unit_full[k % kRing], (k / kRing) & 1, p.err);
+      drained = wait_own(&sm.unit_full[k % kRing], (k / kRing) & 1, p.err);
     return;
   }
 

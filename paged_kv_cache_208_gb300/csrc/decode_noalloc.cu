@@ -27,25 +27,30 @@ static __device__ __align__(256) unsigned char g_decode_scratch[PKV_DECODE_NOALL
 constexpr int kMaxDevices = 64;
 
 struct ScratchSlot {
-  std::once_flag once;
+  std::mutex mu;
   void *ptr = nullptr;
-  bool ok = false;
 };
 ScratchSlot g_scratch[kMaxDevices];
 
 // The device address of the scratch array on the current device. In host code the array's
-// name is only a host-side stand-in, so the address is looked up once per device (with that
-// device current) and cached.
+// name is only a host-side stand-in, so the address is looked up (with that device current)
+// and cached. Only a successful lookup is cached: a failed one (for example made while a
+// stream is being captured) is retried by the next call, and its error is cleared so that
+// it does not surface in the caller's next cudaGetLastError.
 void *scratch_on_current_device() {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
   ScratchSlot &s = g_scratch[dev];
-  std::call_once(s.once, [&] {
+  std::lock_guard<std::mutex> lock(s.mu);
+  if (!s.ptr) {
     void *p = nullptr;
-    s.ok = cudaGetSymbolAddress(&p, g_decode_scratch) == cudaSuccess && p != nullptr;
-    s.ptr = p;
-  });
-  return s.ok ? s.ptr : nullptr;
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) == cudaSuccess && p != nullptr) {
+      s.ptr = p;
+    } else {
+      (void)cudaGetLastError();
+    }
+  }
+  return s.ptr;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

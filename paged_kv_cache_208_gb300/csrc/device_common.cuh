@@ -1,8 +1,10 @@
 // device_common.cuh -- inline-PTX helpers shared by the libpkv kernels (sm_103a).
 //
-// mbarrier pipelines, TMA tensor loads, named barriers, bf16 unpacking and a time-bounded
-// wait. Every wait in the library goes through wait_parity(): after ~2 s without progress it
-// gives up, so a kernel can record PKV_DEVERR_TIMEOUT and return instead of hanging.
+// mbarrier pipelines, TMA tensor loads, named barriers, bf16 unpacking and time-bounded
+// waits. Every wait in the library goes through wait_parity() or wait_own(): after ~2 s
+// without progress it gives up, so a kernel can record PKV_DEVERR_TIMEOUT and return instead
+// of hanging. wait_parity() also gives up at once when another CTA has already timed out;
+// wait_own(), for the CTA's own copies in flight, does not (see there).
 #pragma once
 
 #include <cuda.h>
@@ -74,6 +76,24 @@ __device__ __forceinline__ bool wait_parity(uint64_t *bar, uint32_t parity, unsi
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (aborted(err)) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (err) atomicOr(err, kErrTimeout);
+      return false;
+    }
+  }
+}
+
+// Wait for a copy (TMA, bulk copy) or a tensor-core operation that this CTA issued itself.
+// Unlike wait_parity this ignores the abort bit: an operation that was issued completes
+// unless the context has faulted, and the CTA must not exit, release its tensor memory or
+// reuse the shared memory before it has. It is still bounded by the same time limit.
+__device__ __forceinline__ bool wait_own(uint64_t *bar, uint32_t parity, unsigned int *err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
     if (global_timer_ns() - t0 > kWaitLimitNs) {
       if (err) atomicOr(err, kErrTimeout);
       return false;

@@ -38,13 +38,16 @@ __global__ void __launch_bounds__(32)
     record_error(err, 1u /* PKV_DEVERR_SLOT_RANGE */);
     return;
   }
+  if (aborted(err)) return;  // an earlier wait gave up somewhere: issue nothing
   uint8_t *kb = buf + (size_t)i * 2 * row_bytes, *vb = kb + row_bytes;
   mbar_init(&full[i], 1);  // this thread's own barrier: no other thread touches it
   fence_mbar_init();
   mbar_arrive_expect_tx(&full[i], 2 * row_bytes);
   bulk_copy_g2s(kb, k + t * k_stride, row_bytes, &full[i]);
   bulk_copy_g2s(vb, v + t * v_stride, row_bytes, &full[i]);
-  if (!wait_parity(&full[i], 0, err)) return;
+  // the rows are this thread's own copies: wait for them to land even if another CTA has
+  // given up meanwhile (only the time limit ends this wait)
+  if (!wait_own(&full[i], 0, err)) return;
   bulk_copy_s2g(k_cache + slot * row_bytes, kb, row_bytes);
   bulk_copy_s2g(v_cache + slot * row_bytes, vb, row_bytes);
   bulk_commit();

@@ -93,6 +93,7 @@ struct PrefillSmem {
   uint64_t kv_full[kSlots], kv_empty[kSlots];
   uint64_t v_fixed[kSlots];  // per slot: the next fix of a slot needs that slot released
   uint64_t s_full[2], p_full[2], o_full[2];
+  uint64_t mma_drain;  // the MMA thread's last commit: every UMMA it issued has completed
   uint64_t item_full[kRing], item_empty[kRing];
   Item items[kRing];  // decoded once by the scheduler, read by the other warps
   uint32_t tmem_base;
@@ -267,6 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.p_full[a], 4);
       mbar_init(&sm.o_full[a], 1);
     }
+    mbar_init(&sm.mma_drain, 1);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -294,6 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       pol_kv = policy_evict_last();
     }
     uint32_t pushed = 0, q_loads = 0, g = 0;
+    uint32_t q_issued[2] = {0, 0};  // loads issued into each Q buffer (lane 0's count)
     int last_load = -1;
     bool ok = true;
     const int total_items = lane == 0 ? *p.num_units * p.num_kv_heads * (G >= 2 ? G / 2 : 1) : 0;
@@ -339,6 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int hf = 0; hf < 2; ++hf)
               tma_load_3d(sm.q[a] + hf * kHalfBytes, &qmap, &sm.q_full[a], 0,
                           (int32_t)(it.q0 + it.tok[a]), 2 * it.hq[a] + hf, pol_q);
+            ++q_issued[a];
           }
         }
       }
@@ -394,12 +398,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (lane == 0) {  // keep the CTA alive until every copy issued has landed
+    if (lane == 0) {
+      // keep the CTA alive until every copy issued has landed, also after an abort (these
+      // waits ignore the abort bit; only issued loads are waited for: each Q buffer's last
+      // one, and the K/V loads up to last_load, which were issued in order)
       bool drained = true;
-      for (int a = 0; a < 2 && q_loads > 0; ++a)
-        drained = drained && wait_parity(&sm.q_full[a], (q_loads - 1) & 1, p.err);
+      for (int a = 0; a < 2; ++a)
+        if (q_issued[a] > 0)
+          drained = drained && wait_own(&sm.q_full[a], (q_issued[a] - 1) & 1, p.err);
       for (int t = max(0, last_load - kSlots + 1); drained && t <= last_load; ++t)
-        drained = wait_parity(&sm.kv_full[t % kSlots], (t / kSlots) & 1, p.err);
+        drained = wait_own(&sm.kv_full[t % kSlots], (t / kSlots) & 1, p.err);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ UMMA issuer
@@ -490,8 +498,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ++q_loads;
     }
-    // every UMMA must be complete before the tensor memory is released
-    if (ok && g > 0) wait_all(&sm.o_full[1], (g - 1) & 1);
+    // every UMMA must be complete before the tensor memory is released and the CTA exits,
+    // also after an abort: one more commit tracks all of them (the wait ignores the abort bit)
+    commit_one(&sm.mma_drain);
+    __all_sync(kFull, wait_own(&sm.mma_drain, 0, p.err));
   }
   } else {
     reg_alloc_inc<kSoftmaxRegs>();

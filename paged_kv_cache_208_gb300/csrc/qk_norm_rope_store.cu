@@ -144,6 +144,8 @@ __global__ void __launch_bounds__(kMaxTokensPerCta * 32)
   __syncthreads();
   const int64_t t = (int64_t)blockIdx.x * tokens_per_cta + warp;
   if (warp >= tokens_per_cta || t >= p.num_tokens) return;
+  // an earlier wait gave up somewhere: issue nothing (warp-uniform)
+  if (__any_sync(0xffffffffu, lane == 0 && aborted(p.err))) return;
   uint8_t *row = rows + (size_t)warp * row_bytes;
   if (lane == 0) {
     mbar_arrive_expect_tx(&row_full[warp], row_bytes);
@@ -166,7 +168,8 @@ __global__ void __launch_bounds__(kMaxTokensPerCta * 32)
     cs[2] = src[16 + 2 * gl];
     cs[3] = src[16 + 2 * gl + 1];
   }
-  if (!__all_sync(0xffffffffu, wait_parity(&row_full[warp], 0, p.err))) return;
+  // the warp's own copy: wait for it to land even if another CTA has given up meanwhile
+  if (!__all_sync(0xffffffffu, wait_own(&row_full[warp], 0, p.err))) return;
   if (pos_ok) {
     // query and key heads, eight rows per pass (two per quarter warp); every lane takes part
     // in the shuffles, rows past the key heads contribute zeros

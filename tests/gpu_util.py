@@ -79,3 +79,16 @@ def compact_for_oracle(kc: torch.Tensor, vc: torch.Tensor, tables: np.ndarray):
     v_h = host_bits(vc[idt])
     t2 = np.where(tables >= 0, remap[np.maximum(tables, 0)], -1).astype(np.int32)
     return k_h, v_h, t2
+
+
+def remap_slots(tables: np.ndarray, slots: np.ndarray, block_size: int) -> np.ndarray:
+    """The slots of the blocks `tables` reference, renumbered as compact_for_oracle renumbers
+    the blocks (negative slots stay negative)."""
+    ids = np.unique(tables[tables >= 0])
+    remap = np.full(int(ids.max()) + 1 if len(ids) else 1, -1, np.int64)
+    remap[ids] = np.arange(len(ids))
+    s = np.asarray(slots, np.int64)
+    blk = np.maximum(s, 0) // block_size
+    out = remap[np.minimum(blk, len(remap) - 1)] * block_size + np.maximum(s, 0) % block_size
+    assert (out[s >= 0] >= 0).all(), "a slot outside the referenced blocks"
+    return np.where(s >= 0, out, s).astype(np.int64)

@@ -2,7 +2,8 @@
 path (pkv_kv_store, then pkv_paged_decode_attn): the same output and the same pool, bit for
 bit, for every GQA grouping (groups of 1 and 2 take the fused path, 3 and 4 the store kernel
 first), split settings, padding rows (slot -1, context 0), new K/V given as strided views of a
-fused projection, and the full Qwen3 decode batch; plus the oracle on the tiny step.
+fused projection, and the full Qwen3 decode batch; plus the oracle on the tiny step and on
+the full Qwen3 batch.
 """
 import numpy as np
 import pytest
@@ -10,7 +11,8 @@ import torch
 
 import oracle
 import workloads as w
-from gpu_util import assert_attention_close, dev, fill_sequences_on_device
+from gpu_util import (assert_attention_close, compact_for_oracle, dev, fill_sequences_on_device,
+                      host_bits, remap_slots)
 from libbuild import build_and_import
 
 pytestmark = pytest.mark.gpu
@@ -87,14 +89,23 @@ def test_padding_rows_and_strided_new_kv():
 
 def test_full_qwen3_batch():
     """The benchmark's decode batch (256 sequences, contexts U[100, 2048]) with the automatic
-    split choice: fused step == store + decode, bit for bit."""
+    split choice: fused step == store + decode, bit for bit; and the fused step against the
+    oracle, which stores the same new tokens into its own copy of the referenced blocks and
+    attends over them (every output compared, the stored blocks bit for bit)."""
     lens = w.qwen3_decode_lengths()
     lay = w.qwen3_decode_layout(num_blocks=w.blocks_needed(lens) + 64)
     kc, vc = fill_sequences_on_device(lay, 71)
     q = w.device_bf16_normal((lay.batch, 16, 128), 72)
     kn = w.device_bf16_normal((lay.batch, 8, 128), 73)
     vn = w.device_bf16_normal((lay.batch, 8, 128), 74)
+    k_h, v_h, bt_h = compact_for_oracle(kc, vc, lay.block_tables)   # before the step
     fused, two, pf, pt = _both(lay, kc, vc, q, kn, vn)
     assert _same(fused, two)
     assert _same(pf[0], pt[0]) and _same(pf[1], pt[1])
     assert pkv.get_device_errors() == 0
+    oracle.kv_store(host_bits(kn), host_bits(vn),
+                    remap_slots(lay.block_tables, lay.slot_mapping, lay.block_size), k_h, v_h)
+    ref = oracle.paged_decode(host_bits(q), k_h, v_h, bt_h, lay.context_lens, lay.scale)
+    assert_attention_close(fused, ref, "full Qwen3 batch: oracle")
+    k_after, v_after, _ = compact_for_oracle(pf[0], pf[1], lay.block_tables)
+    assert np.array_equal(k_after, k_h) and np.array_equal(v_after, v_h), "stored rows"

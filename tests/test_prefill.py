@@ -242,9 +242,21 @@ def _sampled_oracle(q_d, k_d, v_d, cq, ck, seqs, block_table=None, kc_d=None, vc
     return outs
 
 
+def _per_quartile(lens, per, seed):
+    """The longest and the shortest sequence, and `per` random sequences from each quartile
+    of the lengths."""
+    order = np.argsort(lens, kind="stable")
+    g = w.rng(seed)
+    picked = {int(order[0]), int(order[-1])}
+    for part in np.array_split(order, 4):
+        picked.update(int(x) for x in g.choice(part, per, replace=False))
+    return sorted(picked)
+
+
 def test_prefill_varlen_full_size():
     """Varlen causal prefill: 256 prompts U[100, 1024] (~143k tokens), packed; the longest,
-    the shortest and four random prompts checked against the oracle."""
+    the shortest and four random prompts of each length quartile checked against the
+    oracle (18 of 256)."""
     lens = w.varlen_prefill_lengths()
     cq = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
     T = int(cq[-1])
@@ -253,8 +265,7 @@ def test_prefill_varlen_full_size():
     v_d = w.device_bf16_normal((T, 8, 128), 403)
     out = pkv.varlen_prefill_attn(q_d, k_d, v_d, dev(cq), dev(cq), int(lens.max()),
                                   int(lens.max()), 128 ** -0.5)
-    seqs = sorted({int(lens.argmax()), int(lens.argmin()),
-                   *w.rng(77).choice(len(lens), 4, replace=False).tolist()})
+    seqs = _per_quartile(lens, 4, 77)
     refs = _sampled_oracle(q_d, k_d, v_d, cq, cq, seqs)
     for n, ref in zip(seqs, refs):
         assert_attention_close(out[int(cq[n]):int(cq[n + 1])], ref, f"seq {n}")
@@ -263,8 +274,9 @@ def test_prefill_varlen_full_size():
 
 def test_prefix_prefill_full_size():
     """Prefix-cached prefill: 64 sequences sharing a 2048-token prefix (8 ref-counted blocks),
-    suffixes U[256, 768]; queries are the suffixes, keys come through block_table. Four
-    sequences checked against the oracle."""
+    suffixes U[256, 768]; queries are the suffixes, keys come through block_table. The
+    longest, the shortest and two random suffixes of each length quartile checked against
+    the oracle (10 of 64)."""
     lay = w.prefix_prefill_case_layout(num_blocks=8 + 64 * 3 + 32)
     assert lay.ref_count.max() == 64
     bs = 256
@@ -281,7 +293,7 @@ def test_prefix_prefill_full_size():
     out = pkv.varlen_prefill_attn(q_d, kc_d, vc_d, dev(cq), dev(ck), int(lay.seqlens_q.max()),
                                   int(lay.seqlens_k.max()), 128 ** -0.5,
                                   block_table=dev(lay.block_table))
-    seqs = [0, 17, 40, 63]
+    seqs = _per_quartile(lay.seqlens_q, 2, 78)
     refs = _sampled_oracle(q_d, None, None, cq, ck, seqs, block_table=lay.block_table,
                            kc_d=kc_d, vc_d=vc_d)
     for n, ref in zip(seqs, refs):
