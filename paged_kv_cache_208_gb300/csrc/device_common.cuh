@@ -87,18 +87,101 @@ __device__ __forceinline__ bool wait_parity(uint64_t *bar, uint32_t parity, unsi
 // Unlike wait_parity this ignores the abort bit: an operation that was issued completes
 // unless the context has faulted, and the CTA must not exit, release its tensor memory or
 // reuse the shared memory before it has. It is still bounded by the same time limit.
-__device__ __forceinline__ bool wait_own(uint64_t *bar, uint32_t parity, unsigned int *err) {
+__device__ __forceinline__ bool wait_own(uint64_t *bar, uint32_t parity, unsigned int *err,
+                                         uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit_ns) {
       if (err) atomicOr(err, kErrTimeout);
       return false;
     }
   }
+}
+
+// ------------------------------------------------------------------ thread-block clusters
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// The shared::cluster address of the variable at shared-memory address `addr` (this CTA's
+// window) in the CTA of the cluster with rank `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t addr, uint32_t rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(addr), "r"(rank));
+  return d;
+}
+
+// All threads of all CTAs of the cluster (every thread of a warp together).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+// Arrive on an mbarrier given by its shared::cluster address (this CTA's or another's), with
+// release semantics at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+                   bar_cluster_addr)
+               : "memory");
+}
+
+// The same with the default (release, CTA scope) semantics: for arrivals that publish no
+// data of their own -- tensor-memory writes ordered by tcgen05.fence::before_thread_sync, or
+// the completion of a copy the arriving thread has observed. Much cheaper than the above on
+// the critical path.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr_, uint4 v) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr_), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr_, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr_), "r"(v) : "memory");
+}
+
+// Non-blocking: has the phase with the given parity completed? (acquire at CTA or cluster
+// scope)
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint64_t *bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// wait_parity for a barrier that threads of another CTA of the cluster arrive on after
+// writing data with remote stores: the phase is polled at CTA scope (cheap) and, once it has
+// completed, acquired once at cluster scope, so what they wrote before arriving is visible.
+__device__ __forceinline__ bool wait_parity_cluster(uint64_t *bar, uint32_t parity,
+                                                    unsigned int *err) {
+  if (!wait_parity(bar, parity, err)) return false;
+  return mbar_test_wait_cluster(bar, parity);
 }
 
 __device__ __forceinline__ uint64_t policy_evict_first() {

@@ -5,31 +5,42 @@
 // table (prefix caching: queries cover only the uncached suffix and the causal mask is
 // aligned to the end of the keys).
 //
-// Persistent kernel: one CTA per SM takes work items from a global queue (an atomic counter
-// in the caller's workspace). A one-CTA planning kernel first writes the work list there:
-// only (sequence, query block) units that have queries, sequences with the most query blocks
-// first and each sequence's blocks heaviest first, all heads of a unit next to each other.
-// The heavy work starts first (the queue balances the SMs), and the query blocks of one
-// sequence run at about the same time, so the K/V tiles they share come from L2. The
-// producer warp takes the items and hands them to the other warps through a small ring in
-// shared memory. An item is
-// one sequence n, one KV head h and two 128-row M-tiles that share every K/V tile: for a GQA
-// group of two (or a pair of heads of a larger group) the two query heads over the same 128
-// tokens; without GQA two consecutive 128-token blocks of the one head. Per 128-key tile j:
-//   S_a = Q_a K_j^T      tcgen05.mma, Q_a and K_j from shared memory, S_a in TMEM
-//   softmax warpgroup a  row max (pass 1) and P_a = 2^(s - m) (pass 2) read from TMEM with
-//                        tcgen05.ld; P_a written back as bf16 over S_a's first 64 columns
-//   O_a += P_a V_j        tcgen05.mma with A = P_a read from TMEM, B = V_j (MN-major) in smem
-// The MMA warp issues S_0(j), O_1 += P_1(j-1) V(j-1), S_1(j), O_0 += P_0(j) V(j), so each
-// softmax warpgroup works while the tensor core serves the other. O_a is rescaled in TMEM
-// only when a row's running max grows by more than 2^8 (its sum l carries the same stale
-// max, so O / l is unchanged).
+// Persistent kernel on CTA pairs (clusters of two CTAs, each on its own SM). A one-CTA
+// planning kernel first writes the work list into the caller's workspace: only (sequence,
+// query block) units that have queries, sequences with the most query blocks first and each
+// sequence's blocks heaviest first, all heads of a unit next to each other, so the heavy work
+// starts first and the query blocks of one sequence run at about the same time (their K/V
+// tiles come from L2). The pair's leader takes items from a global counter and hands them to
+// both CTAs. An item is one sequence n, one KV head h and 256 query rows: for a GQA group of
+// two (or a pair of heads of a larger group) the two query heads over the same 128 tokens,
+// without GQA two consecutive 128-token blocks of the one head; the leader holds the first
+// 128 rows, the peer the other 128. Per 128-key tile j, with M = 256 over the pair:
+//   S(j) = Q K_j^T     tcgen05.mma.cta_group::2: each CTA's 128 Q rows from its own shared
+//                      memory, K_j split by key (leader keys 0-63, peer 64-127), S rows into
+//                      each CTA's tensor memory
+//   softmax            one warpgroup per CTA, thread = row: row max and P = 2^(s - m) read
+//                      from TMEM with tcgen05.ld, P written back as bf16 over S's first 64
+//                      columns
+//   O += P V_j         A = P from each CTA's tensor memory, V_j split by head dimension
+//                      (leader dims 0-63, peer 64-127)
+// S has three buffers in tensor memory, so the tensor core computes S(j+1) and S(j+2) while
+// the softmax works on S(j): S(j+3), which reuses P(j)'s buffer, is issued once PV(j) has
+// completed, across item boundaries. O is rescaled in TMEM only when a row's running max grows
+// by more than 2^8 (its sum l carries the same stale max, so O / l is unchanged). At an item
+// switch the softmax warps first compute the next item's first P, then read the finished O,
+// release it (the next item's first PV waits for that) and write it out, so the tensor core
+// has work queued while the epilogue runs.
 //
-// Warps (384 threads): 0-3 softmax/epilogue of M-tile 0, 4-7 of M-tile 1 (thread = row =
-// TMEM lane), 8 scheduler + TMA producer (Q_0, Q_1 per item, each reloaded as soon as its
-// last S MMA is done; K and V tiles through one 5-slot ring), 9 UMMA issuer and TMEM
-// owner, 10-11 idle. TMEM: S_0 [0,128), S_1 [128,256), O_0 [256,384),
-// O_1 [384,512). Shared memory: Q_0, Q_1 and 5 K/V slots of 32 KiB, 128-byte swizzled.
+// Warps (384 threads per CTA): 0-7 softmax and epilogue (warp w: 16 rows of TMEM lane
+// quadrant w % 4, two threads per row), 8 Q and K loads (Q per item, this CTA's K half per key
+// tile through a 5-slot ring; in the leader also the scheduler), 10 V loads (this CTA's V half
+// per key tile through a 4-slot ring, which lets V tiles, needed three tiles after their K, be
+// loaded later), 9 and 11 in the leader the S and the PV issuers; in the peer warp 9 is a
+// relay that forwards the peer's load completions to the leader's load barriers. All loads are
+// TMA with 128-byte swizzle. Every load lands on a barrier of the CTA that issued it, so each
+// CTA can wait for its own copies before it exits, whatever the other one does.
+// TMEM (512 columns per CTA): S buffers [0,128), [128,256), [256,384), O [384,512). Shared
+// memory per CTA: two Q buffers of 32 KiB, five K and four V slots of 16 KiB.
 //
 // Rows of the last V tile past the sequence's keys are zeroed in shared memory before use
 // (P is 0 there, but 0 x NaN from a stale pool slot would still poison O).
@@ -43,60 +54,67 @@ namespace pkv {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kBM = 128;  // rows of one M-tile
-constexpr int kBN = 128;  // keys per tile
-constexpr int kSlots = 5;  // K/V ring: K(j) is load 2j and V(j) load 2j + 1, slot = load % 5
-constexpr int kThreads = 384;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr uint32_t kTileBytes = kBM * kD * 2;  // 32 KiB
-constexpr uint32_t kHalfBytes = kTileBytes / 2;
+constexpr int kBM = 128;   // query rows per CTA (M = 256 per pair)
+constexpr int kBN = 128;   // keys per tile
+constexpr int kKSlots = 5;  // K ring: K(t) in slot t % 5 (needed by S(t))
+constexpr int kVSlots = 4;  // V ring: V(t) in slot t % 4 (needed by PV(t), three tiles later)
+constexpr int kSBufs = 3;   // S buffers in tensor memory
+constexpr int kSoftmaxWarps = 8;
+constexpr int kKLoadWarp = 8;
+constexpr int kSMmaWarp = 9;   // the relay in the peer
+constexpr int kVLoadWarp = 10;
+constexpr int kPvMmaWarp = 11;  // idle in the peer
+constexpr int kThreads = 12 * 32;
+constexpr uint32_t kQBytes = kBM * kD * 2;     // 32 KiB: one CTA's Q rows
+constexpr uint32_t kQHalf = kQBytes / 2;       // one 64-dim half of them
+constexpr uint32_t kSlotBytes = 16384;         // one CTA's half of a K or V tile
+constexpr uint32_t kKHalf = kSlotBytes / 2;    // one 64-dim half of a K half-tile (64 keys)
 constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kOCol = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr unsigned kFull = 0xffffffffu;
-// Registers per thread: at launch (= 65536 / 384, what __launch_bounds__(384, 1) gives) and
-// after the split. 2 x kSoftmaxRegs + kOtherRegs must not exceed 3 x kLaunchRegs, or the
-// increase would wait forever; the launcher checks the compiled count before every launch.
-constexpr int kLaunchRegs = 168;
-constexpr int kSoftmaxRegs = 208;
-constexpr int kOtherRegs = 88;
-static_assert(2 * kSoftmaxRegs + kOtherRegs <= 3 * kLaunchRegs, "register split too large");
+constexpr int kRing = 8;   // work items in flight between the scheduler and the other warps
+// item_empty arrivals: leader S and PV issuers, V loader and 8 softmax warps; peer K loader,
+// V loader, relay and 8 softmax warps
+constexpr int kItemConsumers = 22;
+constexpr int kSoftmaxArrivals = 2 * kSoftmaxWarps;  // per P / per O release, both CTAs
 
-template <int N>
-__device__ __forceinline__ void reg_alloc_inc() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <int N>
-__device__ __forceinline__ void reg_dealloc() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-
+// A work item as the scheduler hands it out (16 words, copied to both CTAs of the pair).
 struct Item {
-  int id;          // index in the work list; -1 marks the end of the work
-  int n, h;
-  int hq[2];
-  int64_t tok[2];  // first query token (within the sequence) of each M-tile
-  int64_t q0, Lq, k0, Lk;
-  int nk;          // key tiles to process
-  int last_rows;   // keys of the sequence in the last key tile
-  bool valid;      // the item has queries
-  bool bad;        // cu_seqlens / block_table inconsistent for this sequence
+  int32_t id;         // index in the work list; -1 marks the end of the work
+  int32_t n, h;
+  int32_t hq[2];      // query head of the leader's and of the peer's rows
+  int32_t tok[2];     // first query token (within the sequence) of each CTA's rows
+  int32_t q0, Lq, k0, Lk;
+  int32_t nk;         // key tiles to process
+  int32_t last_rows;  // keys of the sequence in the last key tile
+  int32_t valid;      // the item has queries
+  int32_t bad;        // cu_seqlens / block_table inconsistent for this sequence
+  int32_t pad;
 };
-
-constexpr int kRing = 4;  // work items in flight between the scheduler and the other warps
+static_assert(sizeof(Item) == 64, "Item is copied to the peer as four 16-byte words");
 
 struct PrefillSmem {
-  uint8_t q[2][kTileBytes];
-  uint8_t kv[kSlots][kTileBytes];
+  uint8_t q[2][kQBytes];            // 1024-byte aligned (128-byte swizzle atoms)
+  uint8_t k[kKSlots][kSlotBytes];
+  uint8_t v[kVSlots][kSlotBytes];
+  alignas(16) Item items[kRing];    // written by the leader's scheduler into both CTAs
+  // this CTA's loads; in the leader each phase also waits for the relay's arrival, which
+  // says that the peer's half of the same load has landed (two arrivals per phase)
   uint64_t q_full[2], q_empty[2];
-  uint64_t kv_full[kSlots], kv_empty[kSlots];
-  uint64_t v_fixed[kSlots];  // per slot: the next fix of a slot needs that slot released
-  uint64_t s_full[2], p_full[2], o_full[2];
-  uint64_t mma_drain;  // the MMA thread's last commit: every UMMA it issued has completed
+  uint64_t k_full[kKSlots], k_empty[kKSlots], v_full[kVSlots], v_empty[kVSlots];
+  // leader only: the V fixes of both CTAs, the softmax warps' P of each S buffer and their
+  // release of O, the MMA drain
+  uint64_t v_fixed[kVSlots];
+  uint64_t p_full[kSBufs], o_free, mma_drain[2];
+  // both CTAs, committed by the leader's MMA thread: S(t) and PV(t) done, per S buffer t % 3
+  // (a parity wait only tells the current phase from the one before, and the softmax warps
+  // can be two tiles ahead of the last finished PV)
+  uint64_t s_full[kSBufs], o_full[kSBufs];
   uint64_t item_full[kRing], item_empty[kRing];
-  Item items[kRing];  // decoded once by the scheduler, read by the other warps
   uint32_t tmem_base;
+  int32_t stop;                     // the cluster returns at once (an earlier wait gave up)
 };
 
 struct PrefillParams {
@@ -117,10 +135,9 @@ struct PrefillParams {
   int32_t causal;
   uint16_t *out;
   bool out_32b;    // out is 32-byte aligned: rows are written with 32-byte stores
-  int32_t *queue;  // next item to hand out (zeroed before the launch)
+  int32_t *queue;  // next item to hand out (zeroed by the planner)
   unsigned int *err;
 };
-
 
 // Item i of the work list: unit i / (KV heads x head pairs), head pair i % that.
 template <int G>
@@ -128,6 +145,7 @@ __device__ __forceinline__ Item decode_item(const PrefillParams &p, int i) {
   constexpr int kPairs = G >= 2 ? G / 2 : 1;
   Item it;
   it.id = i;
+  it.pad = 0;
   const int per_unit = p.num_kv_heads * kPairs;
   const int2 u = p.units[i / per_unit];
   const int hp = i % per_unit;
@@ -138,91 +156,114 @@ __device__ __forceinline__ Item decode_item(const PrefillParams &p, int i) {
   if (G >= 2) {
     it.hq[0] = it.h * G + 2 * pair;
     it.hq[1] = it.hq[0] + 1;
-    it.tok[0] = it.tok[1] = (int64_t)qb * kBM;
+    it.tok[0] = it.tok[1] = qb * kBM;
   } else {
     it.hq[0] = it.hq[1] = it.h;
-    it.tok[0] = (int64_t)qb * 2 * kBM;
+    it.tok[0] = qb * 2 * kBM;
     it.tok[1] = it.tok[0] + kBM;
   }
-  it.q0 = p.cu_q[it.n];
-  it.Lq = p.cu_q[it.n + 1] - it.q0;
-  it.k0 = p.cu_k[it.n];
-  it.Lk = p.cu_k[it.n + 1] - it.k0;
-  bool bad = it.Lq < 0 || it.Lk < 0 || it.q0 < 0 || it.q0 + it.Lq > p.total_q;
-  if (p.block_table) bad = bad || it.Lk > (int64_t)p.table_width * p.block_size;
-  else bad = bad || it.k0 < 0 || it.k0 + it.Lk > p.kv_rows;
+  const int64_t q0 = p.cu_q[it.n], Lq = p.cu_q[it.n + 1] - q0;
+  const int64_t k0 = p.cu_k[it.n], Lk = p.cu_k[it.n + 1] - k0;
+  bool bad = Lq < 0 || Lk < 0 || q0 < 0 || q0 + Lq > p.total_q;
+  if (p.block_table) bad = bad || Lk > (int64_t)p.table_width * p.block_size;
+  else bad = bad || k0 < 0 || k0 + Lk > p.kv_rows;
+  it.q0 = (int32_t)q0;
+  it.Lq = (int32_t)Lq;
+  it.k0 = (int32_t)k0;
+  it.Lk = (int32_t)Lk;
   it.bad = bad;
-  it.valid = !bad && it.tok[0] < it.Lq;
+  it.valid = !bad && it.tok[0] < Lq;
   it.nk = 0;
   it.last_rows = 0;
   if (it.valid) {
     int64_t kv_end = 0;
 #pragma unroll
     for (int a = 0; a < 2; ++a) {
-      if (it.tok[a] >= it.Lq) continue;
-      const int64_t last_q = min(it.Lq, it.tok[a] + kBM) - 1;
-      const int64_t e = p.causal ? min(it.Lk, last_q + (it.Lk - it.Lq) + 1) : it.Lk;
+      if (it.tok[a] >= Lq) continue;
+      const int64_t last_q = min(Lq, (int64_t)it.tok[a] + kBM) - 1;
+      const int64_t e = p.causal ? min(Lk, last_q + (Lk - Lq) + 1) : Lk;
       kv_end = max(kv_end, e);
     }
     if (kv_end > 0) {
       it.nk = (int)((kv_end + kBN - 1) / kBN);
-      it.last_rows = (int)min((int64_t)kBN, it.Lk - (int64_t)(it.nk - 1) * kBN);
+      it.last_rows = (int)min((int64_t)kBN, Lk - (int64_t)(it.nk - 1) * kBN);
     }
   }
   return it;
 }
 
-// Next work item from the ring (in order), taken by a whole warp: every lane waits, and the
-// item counts only if every lane saw it (so the warp agrees even when a wait gives up).
-// Returns the slot, or nullptr when the wait gave up. The caller reads the fields it needs
-// in place and then releases the slot (release_item).
-__device__ __forceinline__ const Item *wait_item(PrefillSmem &sm, uint32_t taken,
+// Next work item from this CTA's ring (in order), taken by a whole warp: every lane waits,
+// and the item counts only if every lane saw it. In the peer the leader's scheduler wrote
+// the item with remote stores, so the wait acquires at cluster scope there. Returns the
+// slot, or nullptr when the wait gave up.
+__device__ __forceinline__ const Item *wait_item(PrefillSmem &sm, uint32_t taken, bool leader,
                                                  unsigned int *err) {
   const int slot = taken % kRing;
-  if (__all_sync(0xffffffffu, wait_parity(&sm.item_full[slot], (taken / kRing) & 1, err)))
+  const uint32_t par = (taken / kRing) & 1;
+  if (__all_sync(kFull, leader ? wait_parity(&sm.item_full[slot], par, err)
+                               : wait_parity_cluster(&sm.item_full[slot], par, err)))
     return &sm.items[slot];
   return nullptr;
 }
 
-__device__ __forceinline__ void release_item(PrefillSmem &sm, uint32_t taken, int lane) {
-  __syncwarp();  // every lane has read the item before the slot is released
-  if (lane == 0) mbar_arrive(&sm.item_empty[taken % kRing]);
+// Release a ring slot once every lane has read it: one arrival per warp on the leader's
+// item_empty (item_empty_l = its shared::cluster address).
+__device__ __forceinline__ void release_item(uint32_t item_empty_l, uint32_t taken, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive_remote(item_empty_l + (taken % kRing) * 8);
 }
 
-// S = Q K^T for one 128 x 128 tile: 8 UMMAs of K = 16 over the two 64-column halves. The
+// S = Q K^T for one tile over the pair: 8 UMMAs of K = 16 over the two 64-dim halves. The
 // descriptors are the tiles' base descriptors plus compile-time offsets (the start address
-// sits in the low bits, in 16-byte units). Called by the whole MMA warp; one lane issues.
+// sits in the low bits, in 16-byte units). Issued by the MMA warp's elected lane.
 __device__ __forceinline__ void mma_qk(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc,
                                        uint32_t idesc) {
-  if (elect_one()) {
-    umma_ss<false>(d_tmem, q_desc, k_desc, idesc);
+  umma_pair_ss<false>(d_tmem, q_desc, k_desc, idesc);
 #pragma unroll
-    for (int kk = 1; kk < kD / 16; ++kk) {
-      const uint64_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
-      umma_ss<true>(d_tmem, q_desc + off, k_desc + off, idesc);
-    }
+  for (int kk = 1; kk < kD / 16; ++kk) {
+    const uint64_t qoff = ((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4;
+    const uint64_t koff = ((kk >> 2) * kKHalf + (kk & 3) * 32) >> 4;
+    umma_pair_ss<true>(d_tmem, q_desc + qoff, k_desc + koff, idesc);
   }
-  __syncwarp();
 }
 
-// O (+)= P V for one tile: P from TMEM (8 columns per 16 keys), V MN-major in smem (16 keys
-// = 2 KiB further per step).
+// O (+)= P V for one tile: P from TMEM (8 columns per 16 keys), V MN-major in shared memory
+// (16 keys = 2 KiB further per step).
 __device__ __forceinline__ void mma_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc,
                                        uint32_t idesc, bool accumulate) {
-  if (elect_one()) {
-    if (accumulate) umma_ts<true>(d_tmem, p_tmem, v_desc, idesc);
-    else umma_ts<false>(d_tmem, p_tmem, v_desc, idesc);
+  if (accumulate) umma_pair_ts<true>(d_tmem, p_tmem, v_desc, idesc);
+  else umma_pair_ts<false>(d_tmem, p_tmem, v_desc, idesc);
 #pragma unroll
-    for (int kk = 1; kk < kBN / 16; ++kk)
-      umma_ts<true>(d_tmem, p_tmem + 8 * kk, v_desc + ((kk * 16 * 128) >> 4), idesc);
-  }
-  __syncwarp();
+  for (int kk = 1; kk < kBN / 16; ++kk)
+    umma_pair_ts<true>(d_tmem, p_tmem + 8 * kk, v_desc + ((kk * 16 * 128) >> 4), idesc);
 }
 
-// tcgen05.commit from the lane that issued the UMMAs (the warp is converged here too).
-__device__ __forceinline__ void commit_one(uint64_t *bar) {
-  if (elect_one()) umma_commit(bar);
-  __syncwarp();
+// Commits to the barrier at the same offset in both CTAs (bar_l = its address in the leader,
+// bar_p in the peer).
+__device__ __forceinline__ void commit_both(uint32_t bar_l, uint32_t bar_p) {
+  umma_commit_pair(bar_l);
+  umma_commit_pair(bar_p);
+}
+
+// Time limit of the loaders' final waits for their own loads. In the leader a load's phase
+// also needs the relay's arrival for the peer's half; after an abort that arrival may never
+// come, while the leader's own bytes land within microseconds of being issued, so there the
+// wait is cut to 1 ms.
+__device__ __forceinline__ uint64_t drain_limit_ns(const unsigned int *err, bool leader) {
+  return leader && aborted(err) ? 1000000ull : kWaitLimitNs;
+}
+
+// First pool (or packed) row of key tile j of an item; a block id outside the pool is
+// flagged and gives a row wholly outside the tensor (TMA fills zeros there).
+__device__ __forceinline__ int32_t tile_row(const PrefillParams &p, const Item &it, int j) {
+  if (!p.block_table) return it.k0 + j * kBN;
+  const int64_t key = (int64_t)j * kBN;
+  const int64_t blk = p.block_table[(int64_t)it.n * p.table_width + key / p.block_size];
+  if (blk < 0 || blk >= p.num_blocks) {
+    record_error(p.err, 2u /* BLOCK_RANGE */);
+    return -2 * kBN;
+  }
+  return (int32_t)(blk * p.block_size + key % p.block_size);
 }
 
 // One 32-byte global store (sm_100 and later); p must be 32-byte aligned.
@@ -243,329 +284,504 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
   extern __shared__ uint8_t smem_raw[];
   PrefillSmem &sm = *reinterpret_cast<PrefillSmem *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-  // an earlier wait gave up somewhere: return before allocating anything (uniform)
-  if (__syncthreads_or(tid == 0 && aborted(p.err))) return;
   if (tid == 0) {
     for (int a = 0; a < 2; ++a) {
-      mbar_init(&sm.q_full[a], 1);
+      mbar_init(&sm.q_full[a], leader ? 2 : 1);
       mbar_init(&sm.q_empty[a], 1);
     }
+    for (int i = 0; i < kKSlots; ++i) {
+      mbar_init(&sm.k_full[i], leader ? 2 : 1);
+      mbar_init(&sm.k_empty[i], 1);
+    }
+    for (int i = 0; i < kVSlots; ++i) {
+      mbar_init(&sm.v_full[i], leader ? 2 : 1);
+      mbar_init(&sm.v_empty[i], 1);
+      mbar_init(&sm.v_fixed[i], 2);
+    }
+    for (int b = 0; b < kSBufs; ++b) {
+      mbar_init(&sm.s_full[b], 1);
+      mbar_init(&sm.p_full[b], kSoftmaxArrivals);
+      mbar_init(&sm.o_full[b], 1);
+    }
+    mbar_init(&sm.o_free, kSoftmaxArrivals);
+    mbar_init(&sm.mma_drain[0], 1);
+    mbar_init(&sm.mma_drain[1], 1);
     for (int i = 0; i < kRing; ++i) {
       mbar_init(&sm.item_full[i], 1);
-      mbar_init(&sm.item_empty[i], 1 + 8);  // the MMA thread and the 8 softmax warps
+      mbar_init(&sm.item_empty[i], kItemConsumers);
     }
-    for (int i = 0; i < kSlots; ++i) {
-      mbar_init(&sm.kv_full[i], 1);
-      mbar_init(&sm.kv_empty[i], 1);
-      mbar_init(&sm.v_fixed[i], 1);
-    }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(&sm.s_full[a], 1);
-      mbar_init(&sm.p_full[a], 4);
-      mbar_init(&sm.o_full[a], 1);
-    }
-    mbar_init(&sm.mma_drain, 1);
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) {
-    tmem_alloc(&sm.tmem_base, kTmemCols);
-    tmem_relinquish();
+  // Both CTAs have started and initialised their barriers; then the leader decides for the
+  // pair whether an earlier wait gave up (the whole cluster returns before allocating).
+  cluster_sync();
+  if (leader && tid == 0) {
+    const int32_t stop = aborted(p.err) ? 1 : 0;
+    sm.stop = stop;
+    st_cluster_u32(cluster_addr(smem_addr(&sm.stop), 1), (uint32_t)stop);
+  }
+  cluster_sync();
+  if (sm.stop) return;
+  if (warp == kSMmaWarp) {
+    tmem_alloc_pair(&sm.tmem_base, kTmemCols);
+    tmem_relinquish_pair();
   }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = sm.tmem_base;
+  const uint32_t item_empty_l = cluster_addr(smem_addr(&sm.item_empty[0]), 0);
+  const uint32_t p_full_l = cluster_addr(smem_addr(&sm.p_full[0]), 0);
+  const uint32_t o_free_l = cluster_addr(smem_addr(&sm.o_free), 0);
+  constexpr int kPairs = G >= 2 ? G / 2 : 1;
 
-  // Register split (launch: kLaunchRegs x 384 threads): the two softmax warpgroups hold a
-  // whole 128-column S row per thread; warpgroup 2 only schedules, loads and issues MMAs.
-  // Each warpgroup executes one setmaxnreg, and the roles are nested under it.
-  if (warp >= 8) {
-  reg_dealloc<kOtherRegs>();
-  if (warp == kProducerWarp) {
-    // ------------------------------------------------------------- scheduler + TMA producer
+  if (warp == kKLoadWarp) {
+    // ---------------------------------------- scheduler (leader) + Q and K loads (both CTAs)
+    // Lane 0 takes the items (in the leader) and issues the loads; the whole warp runs the
+    // loop so that every lane sees the same decisions.
     uint64_t pol_q = 0, pol_kv = 0;
     if (lane == 0) {
       prefetch_tensormap(&qmap);
       prefetch_tensormap(&kmap);
-      prefetch_tensormap(&vmap);
       pol_q = policy_evict_first();
       pol_kv = policy_evict_last();
     }
-    uint32_t pushed = 0, q_loads = 0, g = 0;
+    uint32_t taken = 0, q_loads = 0, g = 0;
     uint32_t q_issued[2] = {0, 0};  // loads issued into each Q buffer (lane 0's count)
-    int last_load = -1;
+    uint32_t k_issued = 0;          // K loads issued (in tile order)
     bool ok = true;
-    const int total_items = lane == 0 ? *p.num_units * p.num_kv_heads * (G >= 2 ? G / 2 : 1) : 0;
+    const int total_items =
+        (leader && lane == 0) ? *p.num_units * p.num_kv_heads * kPairs : 0;
     while (ok) {
-      // take the next item that has queries; -1 when the queue is exhausted
-      int i = -1;
-      if (lane == 0) {
-        Item d;
-        d.id = -1;
-        while (true) {
-          i = atomicAdd(p.queue, 1);
-          if (i >= total_items) break;
-          d = decode_item<G>(p, i);
-          if (d.bad) record_error(p.err, 8u /* SEQLEN_RANGE */);
-          if (d.valid) break;
+      const int slot = taken % kRing;
+      if (leader) {
+        // take the next item that has queries; id -1 when the queue is exhausted
+        if (lane == 0) {
+          Item d;
+          int i;
+          while (true) {
+            i = atomicAdd(p.queue, 1);
+            if (i >= total_items) break;
+            d = decode_item<G>(p, i);
+            if (d.bad) record_error(p.err, 8u /* SEQLEN_RANGE */);
+            if (d.valid) break;
+          }
+          if (i >= total_items) {
+            d = Item{};
+            d.id = -1;
+          }
+          if (taken >= kRing)
+            ok = wait_parity_cluster(&sm.item_empty[slot], ((taken / kRing) - 1) & 1, p.err);
+          if (ok) {
+            sm.items[slot] = d;
+            const uint32_t dst = cluster_addr(smem_addr(&sm.items[slot]), 1);
+            const uint4 *w4 = reinterpret_cast<const uint4 *>(&d);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) st_cluster_v4(dst + 16 * k, w4[k]);
+            mbar_arrive(&sm.item_full[slot]);  // release: visible to this CTA's waiters
+            mbar_arrive_cluster(cluster_addr(smem_addr(&sm.item_full[slot]), 1));
+          }
         }
-        if (i >= total_items) {
-          i = -1;
-          d.id = -1;
-        }
-        const int slot = pushed % kRing;
-        if (pushed >= kRing)
-          ok = wait_parity(&sm.item_empty[slot], ((pushed / kRing) - 1) & 1, p.err);
-        if (ok) {
-          sm.items[slot] = d;
-          mbar_arrive(&sm.item_full[slot]);  // release: the item is visible to the waiters
-        }
+        ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        __syncwarp();  // lane 0 wrote the slot
+      } else {
+        ok = __all_sync(kFull, wait_parity_cluster(&sm.item_full[slot], (taken / kRing) & 1, p.err));
+        if (!ok) break;
       }
-      ++pushed;
-      ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
-      i = __shfl_sync(kFull, i, 0);
-      if (!ok || i < 0) break;
-      __syncwarp();  // lane 0 wrote the slot
-      const Item it = sm.items[(pushed - 1) % kRing];
+      const Item it = sm.items[slot];
+      if (!leader) release_item(item_empty_l, taken, lane);
+      ++taken;
+      if (it.id < 0) break;
       if (it.nk == 0) continue;  // no key visible: the softmax warps write zeros
       if (lane == 0) {
+        const int qb = q_loads & 1;
+        if (q_loads >= 2) ok = wait_parity(&sm.q_empty[qb], ((q_loads >> 1) - 1) & 1, p.err);
+        if (ok) {
+          mbar_arrive_expect_tx(&sm.q_full[qb], kQBytes);
 #pragma unroll
-        for (int a = 0; a < 2; ++a) {
-          if (q_loads > 0) ok = ok && wait_parity(&sm.q_empty[a], (q_loads - 1) & 1, p.err);
-          if (ok) {
-            mbar_arrive_expect_tx(&sm.q_full[a], kTileBytes);
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf)
-              tma_load_3d(sm.q[a] + hf * kHalfBytes, &qmap, &sm.q_full[a], 0,
-                          (int32_t)(it.q0 + it.tok[a]), 2 * it.hq[a] + hf, pol_q);
-            ++q_issued[a];
+          for (int hf = 0; hf < 2; ++hf)
+            tma_load_3d(sm.q[qb] + hf * kQHalf, &qmap, &sm.q_full[qb], 0,
+                        it.q0 + it.tok[rank], 2 * it.hq[rank] + hf, pol_q);
+          ++q_issued[qb];
+        }
+        for (int j = 0; j < it.nk && ok; ++j, ++g) {
+          const int ks = g % kKSlots;
+          if (g >= kKSlots) ok = wait_parity(&sm.k_empty[ks], ((g / kKSlots) - 1) & 1, p.err);
+          if (ok) {  // this CTA's 64 keys: both 64-dim halves in one box
+            mbar_arrive_expect_tx(&sm.k_full[ks], kSlotBytes);
+            tma_load_3d(sm.k[ks], &kmap, &sm.k_full[ks], 0,
+                        tile_row(p, it, j) + 64 * (int32_t)rank, 2 * it.h, pol_kv);
+            ++k_issued;
           }
         }
       }
       ++q_loads;
       ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+      g = __shfl_sync(kFull, g, 0);
+    }
+    if (lane == 0) {
+      // keep the CTA alive until every copy it issued has landed, also after an abort (these
+      // waits ignore the abort bit; only issued loads are waited for)
+      const uint64_t lim = drain_limit_ns(p.err, leader);
+      bool drained = true;
+      for (int a = 0; a < 2; ++a)
+        if (q_issued[a] > 0)
+          drained = drained && wait_own(&sm.q_full[a], (q_issued[a] - 1) & 1, p.err, lim);
+      for (uint32_t t = k_issued > kKSlots ? k_issued - kKSlots : 0; drained && t < k_issued; ++t)
+        drained = wait_own(&sm.k_full[t % kKSlots], (t / kKSlots) & 1, p.err, lim);
+    }
+    __syncwarp();
+  } else if (warp == kVLoadWarp) {
+    // ---------------------------------------------------------------- V loads (both CTAs)
+    // Follows the items on its own ring, so V tiles (needed three tiles after their K) are
+    // loaded as late as the V ring allows; zeroes the rows of an item's last V tile past
+    // the sequence's keys (the whole warp), then tells the leader's MMA thread.
+    uint64_t pol_kv = 0;
+    if (lane == 0) {
+      prefetch_tensormap(&vmap);
+      pol_kv = policy_evict_last();
+    }
+    const uint32_t v_fixed_l = cluster_addr(smem_addr(&sm.v_fixed[0]), 0);
+    uint32_t taken = 0, g = 0, v_issued = 0;
+    bool ok = true;
+    while (ok) {
+      const Item *ip = wait_item(sm, taken, leader, p.err);
+      if (!ip) break;
+      const Item it = *ip;
+      release_item(item_empty_l, taken, lane);
+      ++taken;
+      if (it.id < 0) break;
       for (int j = 0; j < it.nk && ok; ++j, ++g) {
-        const uint32_t nk_load = 2 * g, nv_load = 2 * g + 1;
-        const int ks = nk_load % kSlots, vs = nv_load % kSlots;
+        const int vs = g % kVSlots;
         if (lane == 0) {
-          int32_t row;
-          if (p.block_table) {
-            const int64_t key = (int64_t)j * kBN;
-            const int64_t blk = p.block_table[(int64_t)it.n * p.table_width + key / p.block_size];
-            if (blk < 0 || blk >= p.num_blocks) {
-              record_error(p.err, 2u /* BLOCK_RANGE */);
-              row = -2 * kBN;  // wholly outside the pool: TMA fills zeros
-            } else {
-              row = (int32_t)(blk * p.block_size + key % p.block_size);
-            }
-          } else {
-            row = (int32_t)(it.k0 + (int64_t)j * kBN);
-          }
-          if (nk_load >= kSlots)
-            ok = wait_parity(&sm.kv_empty[ks], ((nk_load / kSlots) - 1) & 1, p.err);
-          if (ok) {
-            mbar_arrive_expect_tx(&sm.kv_full[ks], kTileBytes);
-            tma_load_3d(sm.kv[ks], &kmap, &sm.kv_full[ks], 0, row, 2 * it.h, pol_kv);
-            last_load = (int)nk_load;
-          }
-          if (ok && nv_load >= kSlots)
-            ok = wait_parity(&sm.kv_empty[vs], ((nv_load / kSlots) - 1) & 1, p.err);
-          if (ok) {
-            mbar_arrive_expect_tx(&sm.kv_full[vs], kTileBytes);
-            tma_load_3d(sm.kv[vs], &vmap, &sm.kv_full[vs], 0, row, 2 * it.h, pol_kv);
-            last_load = (int)nv_load;
+          if (g >= kVSlots) ok = wait_parity(&sm.v_empty[vs], ((g / kVSlots) - 1) & 1, p.err);
+          if (ok) {  // this CTA's 64 dims of all 128 keys
+            mbar_arrive_expect_tx(&sm.v_full[vs], kSlotBytes);
+            tma_load_3d(sm.v[vs], &vmap, &sm.v_full[vs], 0, tile_row(p, it, j),
+                        2 * it.h + (int32_t)rank, pol_kv);
+            ++v_issued;
           }
         }
         ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
         if (ok && j == it.nk - 1 && it.last_rows < kBN) {
-          // zero the rows past the sequence's keys before the MMA reads this V tile
-          ok = __all_sync(kFull, wait_parity(&sm.kv_full[vs], (nv_load / kSlots) & 1, p.err));
+          ok = __all_sync(kFull, wait_parity(&sm.v_full[vs], (g / kVSlots) & 1, p.err));
           if (ok) {
-            uint8_t *vt = sm.kv[vs];
-            for (int idx = lane; idx < (kBN - it.last_rows) * 16; idx += 32) {
-              const int r = it.last_rows + (idx >> 4), c = idx & 15;
-              *reinterpret_cast<uint4 *>(vt + (c >> 3) * kHalfBytes + r * 128 + (c & 7) * 16) =
+            uint8_t *vt = sm.v[vs];
+            for (int idx = lane; idx < (kBN - it.last_rows) * 8; idx += 32)
+              *reinterpret_cast<uint4 *>(vt + (it.last_rows + (idx >> 3)) * 128 + (idx & 7) * 16) =
                   make_uint4(0, 0, 0, 0);
-            }
             fence_async_shared();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.v_fixed[vs]);
+            if (lane == 0) mbar_arrive_cluster(v_fixed_l + vs * 8);
           }
         }
       }
     }
-    if (lane == 0) {
-      // keep the CTA alive until every copy issued has landed, also after an abort (these
-      // waits ignore the abort bit; only issued loads are waited for: each Q buffer's last
-      // one, and the K/V loads up to last_load, which were issued in order)
+    if (lane == 0) {  // drain this CTA's V loads (ignores the abort bit)
+      const uint64_t lim = drain_limit_ns(p.err, leader);
       bool drained = true;
-      for (int a = 0; a < 2; ++a)
-        if (q_issued[a] > 0)
-          drained = drained && wait_own(&sm.q_full[a], (q_issued[a] - 1) & 1, p.err);
-      for (int t = max(0, last_load - kSlots + 1); drained && t <= last_load; ++t)
-        drained = wait_own(&sm.kv_full[t % kSlots], (t / kSlots) & 1, p.err);
+      for (uint32_t t = v_issued > kVSlots ? v_issued - kVSlots : 0; drained && t < v_issued; ++t)
+        drained = wait_own(&sm.v_full[t % kVSlots], (t / kVSlots) & 1, p.err, lim);
     }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------------ UMMA issuer
-    // The whole warp runs this loop (waits, descriptor arithmetic) so that it stays
-    // converged; one elected lane issues each group of UMMAs and its commits.
-    constexpr uint32_t kIdS = idesc_bf16_f32(kBM, kBN, 0, 0);  // Q (K-major) x K (K-major)
-    constexpr uint32_t kIdO = idesc_bf16_f32(kBM, kD, 0, 1);   // P (TMEM) x V (MN-major)
-    constexpr uint64_t kSlotStep = kTileBytes >> 4;            // one ring slot, descriptor units
-    const uint64_t dq0 = smem_desc_sw128(smem_addr(sm.q[0]), 16, 1024);
-    const uint64_t dq1 = smem_desc_sw128(smem_addr(sm.q[1]), 16, 1024);
-    const uint64_t dk0 = smem_desc_sw128(smem_addr(sm.kv[0]), 16, 1024);
-    const uint64_t dv0 = smem_desc_sw128(smem_addr(sm.kv[0]), kHalfBytes, 1024);
-    uint32_t taken = 0, q_loads = 0, g = 0;
-    uint32_t fix_parity = 0;  // bit s: parity of the next v_fixed phase of slot s
-    bool ok = true;
-    // warp-uniform wait
+    __syncwarp();
+  } else if (warp == kSMmaWarp && !leader) {
+    // ------------------------------------------------------------------ relay (peer)
+    // Forward each of this CTA's Q, K and V loads to the leader once it has landed. One lane
+    // polls the three streams (each in load order) without blocking, so a load that lands
+    // early is never held up behind another stream's; it learns the loads from the item
+    // ring and sleeps briefly when nothing is ready. Gives up like a wait: after the time
+    // limit without progress, or at once when the abort bit is set.
+    if (lane == 0) {
+      const uint32_t q_full_l = cluster_addr(smem_addr(&sm.q_full[0]), 0);
+      const uint32_t k_full_l = cluster_addr(smem_addr(&sm.k_full[0]), 0);
+      const uint32_t v_full_l = cluster_addr(smem_addr(&sm.v_full[0]), 0);
+      uint32_t taken = 0, q_known = 0, t_known = 0, q_next = 0, k_next = 0, v_next = 0;
+      bool end = false;
+      uint64_t t0 = global_timer_ns();
+      while (true) {
+        bool progressed = false;
+        if (!end && mbar_test_wait(&sm.item_full[taken % kRing], (taken / kRing) & 1) &&
+            mbar_test_wait_cluster(&sm.item_full[taken % kRing], (taken / kRing) & 1)) {
+          const Item &it = sm.items[taken % kRing];
+          const int id = it.id, nk = it.nk;
+          mbar_arrive_remote(item_empty_l + (taken % kRing) * 8);
+          ++taken;
+          if (id < 0) {
+            end = true;
+          } else if (nk > 0) {
+            ++q_known;
+            t_known += nk;
+          }
+          progressed = true;
+        }
+        if (q_next < q_known && mbar_test_wait(&sm.q_full[q_next & 1], (q_next >> 1) & 1)) {
+          mbar_arrive_remote(q_full_l + (q_next & 1) * 8);
+          ++q_next;
+          progressed = true;
+        }
+        if (k_next < t_known &&
+            mbar_test_wait(&sm.k_full[k_next % kKSlots], (k_next / kKSlots) & 1)) {
+          mbar_arrive_remote(k_full_l + (k_next % kKSlots) * 8);
+          ++k_next;
+          progressed = true;
+        }
+        if (v_next < t_known &&
+            mbar_test_wait(&sm.v_full[v_next % kVSlots], (v_next / kVSlots) & 1)) {
+          mbar_arrive_remote(v_full_l + (v_next % kVSlots) * 8);
+          ++v_next;
+          progressed = true;
+        }
+        if (end && q_next == q_known && k_next == t_known && v_next == t_known) break;
+        if (progressed) {
+          t0 = global_timer_ns();
+        } else {
+          if (aborted(p.err)) break;
+          if (global_timer_ns() - t0 > kWaitLimitNs) {
+            record_error(p.err, kErrTimeout);
+            break;
+          }
+          __nanosleep(32);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (leader && (warp == kSMmaWarp || warp == kPvMmaWarp)) {
+    // ------------------------------------------------------------- UMMA issuers (leader)
+    // Two warps on different SM sub-partitions: one issues S = Q K^T for every tile, the other
+    // O += P V. S(t) reuses the tensor-memory buffer of P(t - 3), so the S warp waits for
+    // PV(t - 3) to complete first. Each warp runs its loop converged and one elected lane
+    // issues a step's UMMAs and commits (commits track the issuing thread's UMMAs; the warp
+    // is converged at every elect, so it is always the same lane).
+    const bool s_role = warp == kSMmaWarp;
+    uint64_t *drain_bar = s_role ? &sm.mma_drain[0] : &sm.mma_drain[1];
     auto wait_all = [&](uint64_t *bar, uint32_t parity) -> bool {
       return __all_sync(kFull, wait_parity(bar, parity, p.err));
     };
-    // V(j) of tile gg: wait for the load (or, for a fixed last tile, for the fix)
-    auto v_ready = [&](uint32_t gg, bool fixed) -> bool {
-      const uint32_t n = 2 * gg + 1, vs = n % kSlots;
-      if (fixed) {
-        const bool r = wait_all(&sm.v_fixed[vs], (fix_parity >> vs) & 1);
-        fix_parity ^= 1u << vs;
-        return r;
-      }
-      return wait_all(&sm.kv_full[vs], (n / kSlots) & 1);
-    };
-    while (ok) {
-      const Item *ip = wait_item(sm, taken, p.err);
-      const int id = ip ? ip->id : -1, nk = ip ? ip->nk : 0;
-      const bool fix_v = ip && ip->last_rows < kBN;
-      release_item(sm, taken, lane);
-      ++taken;
-      if (id < 0) break;
-      if (nk == 0) continue;
-      for (int j = 0; j < nk; ++j, ++g) {
-        const uint32_t ks = (2 * g) % kSlots;
-        ok = wait_all(&sm.kv_full[ks], ((2 * g) / kSlots) & 1);
-        if (!ok) break;
-        tc_fence_after_sync();
-        // S_0(j)
-        if (j == 0) {
-          ok = wait_all(&sm.q_full[0], q_loads & 1);
+    const uint32_t o_full_l = cluster_addr(smem_addr(&sm.o_full[0]), 0);
+    const uint32_t o_full_p = cluster_addr(smem_addr(&sm.o_full[0]), 1);
+    uint32_t taken = 0;
+    bool ok = true;
+    if (s_role) {
+      constexpr uint32_t kIdS = idesc_bf16_f32(2 * kBM, kBN, 0, 0);  // Q (K-major) x K (K-major)
+      const uint64_t dq0 = smem_desc_sw128(smem_addr(sm.q[0]), 16, 1024);
+      const uint64_t dq1 = smem_desc_sw128(smem_addr(sm.q[1]), 16, 1024);
+      const uint64_t dk0 = smem_desc_sw128(smem_addr(sm.k[0]), 16, 1024);
+      const uint32_t s_full_l = cluster_addr(smem_addr(&sm.s_full[0]), 0);
+      const uint32_t s_full_p = cluster_addr(smem_addr(&sm.s_full[0]), 1);
+      const uint32_t k_empty_l = cluster_addr(smem_addr(&sm.k_empty[0]), 0);
+      const uint32_t k_empty_p = cluster_addr(smem_addr(&sm.k_empty[0]), 1);
+      const uint32_t q_empty_l = cluster_addr(smem_addr(&sm.q_empty[0]), 0);
+      const uint32_t q_empty_p = cluster_addr(smem_addr(&sm.q_empty[0]), 1);
+      uint32_t t = 0, items_nz = 0, q_use0 = 0, q_use1 = 0;
+      while (ok) {
+        const Item *ip = wait_item(sm, taken, leader, p.err);
+        const int id = ip ? ip->id : -1, nk = ip ? ip->nk : 0;
+        release_item(item_empty_l, taken, lane);
+        ++taken;
+        if (!ip) {
+          ok = false;
+          break;
+        }
+        if (id < 0) break;
+        if (nk == 0) continue;
+        const int qb = items_nz & 1;
+        ++items_nz;
+        const uint32_t q_use = qb ? q_use1 : q_use0;
+        for (int j = 0; j < nk && ok; ++j, ++t) {
+          const uint32_t ks = t % kKSlots, sb = t % kSBufs;
+          ok = wait_all(&sm.k_full[ks], (t / kKSlots) & 1);
+          if (ok && j == 0) ok = wait_all(&sm.q_full[qb], q_use & 1);
+          // the buffer's previous P has been read by its PV
+          if (ok && t >= kSBufs) ok = wait_all(&sm.o_full[sb], ((t - kSBufs) / kSBufs) & 1);
           if (!ok) break;
           tc_fence_after_sync();
+          const bool last = j == nk - 1;
+          if (elect_one()) {
+            mma_qk(tmem + 128 * sb, qb ? dq1 : dq0, dk0 + ks * (kSlotBytes >> 4), kIdS);
+            commit_both(s_full_l + 8 * sb, s_full_p + 8 * sb);
+            commit_both(k_empty_l + 8 * ks, k_empty_p + 8 * ks);
+            if (last) commit_both(q_empty_l + 8 * qb, q_empty_p + 8 * qb);
+          }
+          __syncwarp();
         }
-        mma_qk(tmem, dq0, dk0 + ks * kSlotStep, kIdS);
-        commit_one(&sm.s_full[0]);
-        if (j == nk - 1) commit_one(&sm.q_empty[0]);
-        // O_1 += P_1(j-1) V(j-1)  (never the last tile here)
-        if (j > 0) {
-          const uint32_t gp = g - 1, vs = (2 * gp + 1) % kSlots;
-          ok = wait_all(&sm.p_full[1], gp & 1) && v_ready(gp, false);
+        if (qb) ++q_use1;
+        else ++q_use0;
+      }
+    } else {
+      constexpr uint32_t kIdO = idesc_bf16_f32(2 * kBM, kD, 0, 1);  // P (TMEM) x V (MN-major)
+      const uint64_t dv0 = smem_desc_sw128(smem_addr(sm.v[0]), kSlotBytes, 1024);
+      const uint32_t v_empty_l = cluster_addr(smem_addr(&sm.v_empty[0]), 0);
+      const uint32_t v_empty_p = cluster_addr(smem_addr(&sm.v_empty[0]), 1);
+      uint32_t t = 0, items = 0;
+      uint32_t fix_parity = 0;  // bit s: parity of the next v_fixed phase of slot s
+      while (ok) {
+        const Item *ip = wait_item(sm, taken, leader, p.err);
+        const int id = ip ? ip->id : -1, nk = ip ? ip->nk : 0;
+        const bool fix = ip && ip->last_rows < kBN;
+        release_item(item_empty_l, taken, lane);
+        ++taken;
+        if (!ip) {
+          ok = false;
+          break;
+        }
+        if (id < 0) break;
+        if (nk == 0) continue;
+        for (int j = 0; j < nk && ok; ++j, ++t) {
+          const uint32_t pb = t % kSBufs, vs = t % kVSlots;
+          ok = wait_all(&sm.p_full[pb], (t / kSBufs) & 1);
+          // the item's first PV overwrites O: the previous item's O must have been read
+          if (ok && j == 0 && items > 0) ok = wait_all(&sm.o_free, (items - 1) & 1);
+          // V(t) landed in both CTAs; for an item's last tile with rows past the keys, both
+          // CTAs have also zeroed them
+          if (ok) ok = wait_all(&sm.v_full[vs], (t / kVSlots) & 1);
+          if (ok && fix && j == nk - 1) {
+            ok = __all_sync(kFull, wait_parity_cluster(&sm.v_fixed[vs], (fix_parity >> vs) & 1,
+                                                       p.err));
+            fix_parity ^= 1u << vs;
+          }
           if (!ok) break;
           tc_fence_after_sync();
-          mma_pv(tmem + 384, tmem + 128, dv0 + vs * kSlotStep, kIdO, j - 1 > 0);
-          commit_one(&sm.o_full[1]);
-          commit_one(&sm.kv_empty[vs]);
+          if (elect_one()) {
+            mma_pv(tmem + kOCol, tmem + 128 * pb, dv0 + vs * (kSlotBytes >> 4), kIdO, j > 0);
+            commit_both(o_full_l + 8 * pb, o_full_p + 8 * pb);
+            commit_both(v_empty_l + 8 * vs, v_empty_p + 8 * vs);
+          }
+          __syncwarp();
         }
-        // S_1(j)
-        if (j == 0) {
-          ok = wait_all(&sm.q_full[1], q_loads & 1);
-          if (!ok) break;
-          tc_fence_after_sync();
-        }
-        mma_qk(tmem + 128, dq1, dk0 + ks * kSlotStep, kIdS);
-        commit_one(&sm.s_full[1]);
-        if (j == nk - 1) commit_one(&sm.q_empty[1]);
-        commit_one(&sm.kv_empty[ks]);
-        // O_0 += P_0(j) V(j); for a fixed last tile this wait also covers O_1's use below
-        ok = wait_all(&sm.p_full[0], g & 1) && v_ready(g, j == nk - 1 && fix_v);
-        if (!ok) break;
-        tc_fence_after_sync();
-        mma_pv(tmem + 256, tmem, dv0 + ((2 * g + 1) % kSlots) * kSlotStep, kIdO, j > 0);
-        commit_one(&sm.o_full[0]);
+        ++items;
       }
-      if (!ok) break;
-      {  // O_1 += P_1(last) V(last): V(last) is ready (waited above)
-        const uint32_t gp = g - 1, vs = (2 * gp + 1) % kSlots;
-        ok = wait_all(&sm.p_full[1], gp & 1);
-        if (!ok) break;
-        tc_fence_after_sync();
-        mma_pv(tmem + 384, tmem + 128, dv0 + vs * kSlotStep, kIdO, nk > 1);
-        commit_one(&sm.o_full[1]);
-        commit_one(&sm.kv_empty[vs]);
-      }
-      ++q_loads;
     }
-    // every UMMA must be complete before the tensor memory is released and the CTA exits,
-    // also after an abort: one more commit tracks all of them (the wait ignores the abort bit)
-    commit_one(&sm.mma_drain);
-    __all_sync(kFull, wait_own(&sm.mma_drain, 0, p.err));
-  }
-  } else {
-    reg_alloc_inc<kSoftmaxRegs>();
+    // every UMMA must be complete before the tensor memory is released and the pair exits,
+    // also after an abort: one more commit tracks all of this warp's (the wait ignores the
+    // abort bit)
+    if (elect_one()) umma_commit_pair(cluster_addr(smem_addr(drain_bar), 0));
+    __syncwarp();
+    __all_sync(kFull, wait_own(drain_bar, 0, p.err));
+  } else if (warp < kSoftmaxWarps) {
     // ------------------------------------------------------------------ softmax warps
-    const int a = warp >> 2;        // M-tile
-    const int r = tid & (kBM - 1);  // row == TMEM lane
-    const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    const uint32_t s_col = 128 * a, o_col = 256 + 128 * a;
+    // Warp w owns 16 rows: TMEM lanes 16 (w / 4) .. + 16 of lane quadrant w % 4. Two threads
+    // share a row (tcgen05.ld/st shape 16x32bx2): thread i and i + 16 hold its key columns
+    // 0-63 and 64-127 of every tile, and combine the row max (per tile) and the row sum (per
+    // item) with one shuffle. The warps never wait for each other.
+    const int quad = warp & 3, lh = warp >> 2;
+    const int ch = lane >> 4;                             // this thread's column half
+    const int r = quad * 32 + lh * 16 + (lane & 15);      // row == TMEM lane
+    const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32 + lh * 16) << 16);
     const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
     uint32_t taken = 0, g = 0;
     bool ok = true;
+    // the previous item's rows, written out after the next item's first P
+    bool pend = false;
+    int64_t pend_row = -1;
+    float pend_l = 0.f;
+    uint32_t pend_g = 0;
+    // O of the pending item: wait for its last PV, read this thread's half of the row,
+    // release O, write the half row
+    auto epilogue = [&]() -> bool {
+      const float l = pend_l + __shfl_xor_sync(kFull, pend_l, 16);
+      if (!__all_sync(kFull, wait_parity(&sm.o_full[pend_g % kSBufs], (pend_g / kSBufs) & 1,
+                                         p.err)))
+        return false;
+      tc_fence_after_sync();
+      uint32_t o[2][32];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) tmem_ld16x2_32<64>(lane_addr + kOCol + 32 * c, o[c]);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) tmem_ld_wait(o[c]);
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(o_free_l);
+      if (pend_row >= 0) {
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        uint4 *dst = reinterpret_cast<uint4 *>(p.out + pend_row * kD + 64 * ch);
+        // a thread writes its own half row: one 32-byte sector per store when out allows it
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            uint32_t w[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              w[k] = pack_bf16(__uint_as_float(o[c][16 * e + 2 * k]) * inv,
+                               __uint_as_float(o[c][16 * e + 2 * k + 1]) * inv);
+            uint4 *d = dst + c * 4 + 2 * e;
+            if (p.out_32b) {
+              st_global_32b(d, w);
+            } else {
+              d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+              d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            }
+          }
+      }
+      pend = false;
+      return true;
+    };
     while (ok) {
-      const Item *ip = wait_item(sm, taken, p.err);
+      const Item *ip = wait_item(sm, taken, leader, p.err);
       const int id = ip ? ip->id : -1, nk = ip ? ip->nk : 0;
       int64_t row = -1;  // output row (token x head) of this thread; -1 past the queries
       int64_t lim = -1;  // last key this row sees (-1: none)
       if (id >= 0) {
-        const int64_t qi = ip->tok[a] + r, Lq = ip->Lq, Lk = ip->Lk;
+        const int64_t qi = (int64_t)ip->tok[rank] + r, Lq = ip->Lq, Lk = ip->Lk;
         if (qi < Lq) {
-          row = (ip->q0 + qi) * p.num_q_heads + ip->hq[a];
+          row = ((int64_t)ip->q0 + qi) * p.num_q_heads + ip->hq[rank];
           lim = min(p.causal ? qi + (Lk - Lq) : Lk - 1, Lk - 1);
         }
       }
-      release_item(sm, taken, lane);
+      release_item(item_empty_l, taken, lane);
       ++taken;
-      if (id < 0) break;
-      const bool row_valid = row >= 0;
-      uint4 *dst = reinterpret_cast<uint4 *>(p.out + (row_valid ? row : 0) * kD);
+      if (!ip) break;
+      if (id < 0) {
+        if (pend) ok = epilogue();
+        break;
+      }
       if (nk == 0) {  // no key is visible to any row: zeros
-        if (row_valid)
-          for (int c = 0; c < 16; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+        if (row >= 0) {
+          uint4 *dst = reinterpret_cast<uint4 *>(p.out + row * kD + 64 * ch);
+          for (int c = 0; c < 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+        }
         continue;
       }
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = 0; j < nk; ++j, ++g) {
+        const uint32_t sb = g % kSBufs, s_col = 128 * sb;
         // warp-uniform results: the TMEM loads and stores below are .sync.aligned
-        ok = __all_sync(kFull, wait_parity(&sm.s_full[a], g & 1, p.err));
+        ok = __all_sync(kFull, wait_parity(&sm.s_full[sb], (g / kSBufs) & 1, p.err));
         if (!ok) break;
         tc_fence_after_sync();
-        const int64_t rel = lim - (int64_t)j * kBN;  // last visible column of this tile
-        const int lim_rel = (int)(rel < -1 ? -1 : (rel > kBN ? kBN : rel));
+        // last visible column of this thread's half of the tile
+        const int64_t rel = lim - (int64_t)j * kBN - 64 * ch;
+        const int lim_rel = (int)(rel < -1 ? -1 : (rel > 64 ? 64 : rel));
 
-        // the whole S row in registers: one TMEM round trip per tile
-        uint32_t x[4][32];
+        uint32_t x[2][32];  // key columns 64 ch + 32 c + e
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(lane_addr + s_col + 32 * c, x[c]);
+        for (int c = 0; c < 2; ++c) tmem_ld16x2_32<64>(lane_addr + s_col + 32 * c, x[c]);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld_wait(x[c]);
-        if (lim_rel < kBN - 1) {  // diagonal or last tile: columns past lim_rel are -inf
+        for (int c = 0; c < 2; ++c) tmem_ld_wait(x[c]);
+        if (lim_rel < 63) {  // diagonal or last tile: columns past lim_rel are -inf
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < 2; ++c)
 #pragma unroll
             for (int e = 0; e < 32; ++e)
               if (32 * c + e > lim_rel) x[c][e] = __float_as_uint(-INFINITY);
         }
-        float mx[4];
+        float mx[2];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           mx[c] = -INFINITY;
 #pragma unroll
           for (int e = 0; e < 32; e += 2)
             mx[c] = fmax3(mx[c], __uint_as_float(x[c][e]), __uint_as_float(x[c][e + 1]));
         }
-        const float m_tile = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * p.scale_log2;
+        float m_tile = fmaxf(mx[0], mx[1]);
+        m_tile = fmaxf(m_tile, __shfl_xor_sync(kFull, m_tile, 16)) * p.scale_log2;
         const float m_new = fmaxf(m_run, m_tile);
         const bool rescale = m_new > m_run + kRescaleLog2;
         float alpha = 1.f;
@@ -576,27 +792,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
 
-        // O_a holds the tiles before this one: rescale it (never on the first tile)
+        // O holds the item's tiles before this one: rescale it (never on the first tile)
         if (j > 0 && __any_sync(kFull, rescale)) {
-          ok = __all_sync(kFull, wait_parity(&sm.o_full[a], (g - 1) & 1, p.err));
+          ok = __all_sync(kFull, wait_parity(&sm.o_full[(g - 1) % kSBufs],
+                                             ((g - 1) / kSBufs) & 1, p.err));
           if (!ok) break;
           tc_fence_after_sync();
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < 2; ++c) {
             uint32_t o[32];
-            tmem_ld32(lane_addr + o_col + 32 * c, o);
+            tmem_ld16x2_32<64>(lane_addr + kOCol + 32 * c, o);
             tmem_ld_wait(o);
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(lane_addr + o_col + 32 * c, o);
+            tmem_st16x2_32<64>(lane_addr + kOCol + 32 * c, o);
           }
         }
 
-        // P = 2^(s * scale_log2 - m) as bf16 pairs over the first 64 columns of S
+        // P = 2^(s * scale_log2 - m) as bf16 pairs (two keys per column) over the first 64
+        // columns of S: this warp has read all of its rows' S columns, so it may overwrite them
         const float2 nm2 = make_float2(neg_m, neg_m);
         float2 rs0 = make_float2(0.f, 0.f), rs1 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
@@ -607,55 +825,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             else rs0 = fadd2(rs0, pe);
             pk[e] = pack_bf16(pe.x, pe.y);
           }
-          tmem_st16(lane_addr + s_col + 16 * c, pk);
+          tmem_st16x2_16<32>(lane_addr + s_col + 16 * c, pk);
         }
         tmem_st_wait();
         l_run += (rs0.x + rs0.y) + (rs1.x + rs1.y);
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.p_full[a]);
-      }
-      if (!ok) break;
-      // ---- epilogue: O / l -> bf16 rows
-      ok = __all_sync(kFull, wait_parity(&sm.o_full[a], (g - 1) & 1, p.err));
-      if (!ok) break;
-      tc_fence_after_sync();
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t o[32];
-        tmem_ld32(lane_addr + o_col + 32 * c, o);
-        tmem_ld_wait(o);
-        if (row_valid) {
-          // a thread writes its own row: one 32-byte sector per store when out allows it
-          // (a warp's store touches 32 rows, so fewer and wider stores leave the load/store
-          // queue free sooner for the TMEM, shared-memory and UMMA traffic behind them)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            uint32_t w[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              w[k] = pack_bf16(__uint_as_float(o[16 * e + 2 * k]) * inv,
-                               __uint_as_float(o[16 * e + 2 * k + 1]) * inv);
-            uint4 *d = dst + c * 4 + 2 * e;
-            if (p.out_32b) {
-              st_global_32b(d, w);
-            } else {
-              d[0] = make_uint4(w[0], w[1], w[2], w[3]);
-              d[1] = make_uint4(w[4], w[5], w[6], w[7]);
-            }
-          }
+        if (lane == 0) mbar_arrive_remote(p_full_l + sb * 8);
+        // the previous item's O, now that this item's first P is on its way
+        if (j == 0 && pend) {
+          ok = epilogue();
+          if (!ok) break;
         }
       }
+      if (!ok) break;
+      pend = true;
+      pend_row = row;
+      pend_l = l_run;
+      pend_g = g - 1;
     }
   }
 
+  // every role is done with its own copies and UMMAs; the pair leaves together (remote
+  // arrivals and UMMAs touch the other CTA's memory until then)
+  __syncwarp();
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == kMmaWarp) {
-    tc_fence_after_sync();
-    tmem_dealloc(tmem, kTmemCols);
-  }
+  cluster_sync();
+  tc_fence_after_sync();
+  if (warp == kSMmaWarp) tmem_dealloc_pair(tmem, kTmemCols);
 }
 
 // ---------------------------------------------------------------------- work-list planner
@@ -767,39 +965,53 @@ cudaError_t launch_g(const PrefillArgs &a, PrefillParams prm, int num_sms, cudaS
   constexpr int kPairs = G >= 2 ? G / 2 : 1;
   constexpr int kTokensPerItem = G >= 2 ? kBM : 2 * kBM;
   CUtensorMap qm, km, vm;
+  // q: {64 dims, tokens, 2 halves per head}; a CTA loads its 128 rows of one head per half
   const uint64_t qdims[3] = {64, (uint64_t)a.total_q, (uint64_t)a.num_q_heads * 2};
   const uint64_t qstr[2] = {(uint64_t)a.q_tok_stride * 2, 128};
   const uint32_t qbox[3] = {64, (uint32_t)kBM, 1};
+  // k, v: {64 dims, rows, 2 halves per head}; a CTA loads 64 keys x both halves of K and
+  // 128 keys x its half of V
   const uint64_t kvdims[3] = {64, (uint64_t)(a.kv_rows > 0 ? a.kv_rows : 1),
                               (uint64_t)a.num_kv_heads * 2};
   const uint64_t kvstr[2] = {(uint64_t)a.kv_tok_stride * 2, 128};
-  const uint32_t kvbox[3] = {64, (uint32_t)kBN, 2};
+  const uint32_t kbox[3] = {64, (uint32_t)kBN / 2, 2};
+  const uint32_t vbox[3] = {64, (uint32_t)kBN, 1};
   if (encode_tensor_map(&qm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(a.q), qdims,
                         qstr, qbox, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B) != CUDA_SUCCESS ||
       encode_tensor_map(&km, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(a.k), kvdims,
-                        kvstr, kvbox, CU_TENSOR_MAP_SWIZZLE_128B,
+                        kvstr, kbox, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B) != CUDA_SUCCESS ||
       encode_tensor_map(&vm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(a.v), kvdims,
-                        kvstr, kvbox, CU_TENSOR_MAP_SWIZZLE_128B,
+                        kvstr, vbox, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   const size_t smem = sizeof(PrefillSmem) + 1024;
-  static bool configured[64] = {};
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // the pairs that fit on the device at once (one CTA per SM), looked up once per device
+  static int max_pairs[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !configured[dev]) {
-    // The register split inside the kernel draws on the registers the CTA is launched with;
-    // never launch a build whose count cannot cover it (the increase would never return).
-    cudaFuncAttributes fa{};
-    cudaError_t e = cudaFuncGetAttributes(&fa, prefill_kernel<G>);
+  int pairs = dev < 64 ? max_pairs[dev] : 0;
+  if (pairs <= 0) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    if (fa.numRegs * kThreads < (2 * kSoftmaxRegs + kOtherRegs) * 128)
-      return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(prefill_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
+    cfg.gridDim = dim3(2 * (unsigned)(num_sms / 2));
+    e = cudaOccupancyMaxActiveClusters(&pairs, prefill_kernel<G>, &cfg);
     if (e != cudaSuccess) return e;
-    configured[dev] = true;
+    if (pairs <= 0) return cudaErrorInvalidConfiguration;
+    if (dev < 64) max_pairs[dev] = pairs;
   }
   const PrefillWorkspace wl = prefill_workspace_layout(a.num_seqs, a.max_seqlen_q);
   uint8_t *ws = static_cast<uint8_t *>(a.workspace);
@@ -823,12 +1035,12 @@ cudaError_t launch_g(const PrefillArgs &a, PrefillParams prm, int num_sms, cudaS
   const int64_t items = wl.max_units * a.num_kv_heads * kPairs;  // an upper bound
   if (items <= 0) return cudaSuccess;
   if (items > INT32_MAX) return cudaErrorInvalidValue;
-  const unsigned grid = (unsigned)(items < num_sms ? items : num_sms);
+  const int64_t clusters = items < pairs ? items : pairs;
   prefill_plan_kernel<<<1, kPlanThreads, 0, stream>>>(pp);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  prefill_kernel<G><<<grid, kThreads, smem, stream>>>(qm, km, vm, prm);
-  return cudaGetLastError();
+  cfg.gridDim = dim3(2 * (unsigned)clusters);
+  return cudaLaunchKernelEx(&cfg, prefill_kernel<G>, qm, km, vm, prm);
 }
 
 }  // namespace
@@ -838,6 +1050,8 @@ bool prefill_group_supported(int group) {
 }
 
 cudaError_t launch_varlen_prefill(const PrefillArgs &a, int num_sms, cudaStream_t stream) {
+  // token and row indices travel as 32-bit TMA coordinates and item fields
+  if (a.total_q > INT32_MAX || a.kv_rows > INT32_MAX) return cudaErrorInvalidValue;
   PrefillParams prm{};
   prm.cu_q = a.cu_seqlens_q;
   prm.cu_k = a.cu_seqlens_k;

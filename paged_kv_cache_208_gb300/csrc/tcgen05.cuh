@@ -1,6 +1,7 @@
-// tcgen05.cuh -- inline-PTX wrappers for the 5th-generation tensor cores (sm_100 family):
-// tensor-memory allocation, UMMA issue/commit, TMEM loads and stores, and the shared-memory
-// matrix and instruction descriptors for bf16 operands with 128-byte swizzle.
+// tcgen05.cuh -- inline-PTX wrappers for the 5th-generation tensor cores (sm_100 family) as a
+// CTA pair uses them: tensor-memory allocation, UMMA issue/commit, TMEM loads and stores, and
+// the shared-memory matrix and instruction descriptors for bf16 operands with 128-byte
+// swizzle.
 #pragma once
 
 #include <stdint.h>
@@ -9,20 +10,25 @@
 
 namespace pkv {
 
+// Every tcgen05 instruction of a kernel uses the same CTA group. The kernels here run on CTA
+// pairs (a cluster of two CTAs on two SMs): allocation and release are done by one warp of
+// each CTA together, and one thread of the pair's leader (cluster rank 0) issues UMMAs that
+// read both CTAs' shared memory and write both CTAs' tensor memory.
+
 // ------------------------------------------------------------------ tensor memory
-__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                    smem_addr(dst_smem)),
                "r"(ncols)
                : "memory");
 }
 
-__device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                : "memory");
 }
 
@@ -34,65 +40,46 @@ __device__ __forceinline__ void tc_fence_after_sync() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Make this thread's generic-proxy shared-memory writes visible to the async proxy (UMMA).
-
-// ------------------------------------------------------------------ UMMA
-// D[tmem] (+)= A[smem desc] * B[smem desc], kind::f16 (bf16 in, fp32 accumulate), 1 CTA.
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                          uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem desc]: A is read from tensor memory (M rows = lanes, each
-// 32-bit column holding two consecutive bf16 of K), B from shared memory.
-__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
-                                                 uint64_t b_desc, uint32_t idesc,
-                                                 uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// The same two forms with the accumulate flag fixed at compile time (an immediate predicate).
+// ------------------------------------------------------------------ UMMA (CTA pair)
+// D[tmem] (+)= A * B, kind::f16 (bf16 in, fp32 accumulate), M = 256 over the pair: the
+// leader's A rows (its shared memory or, in the _ts form, its tensor memory) are rows
+// 0..127 and land in its tensor memory, the peer's are rows 128..255 and land in the peer's;
+// each CTA holds half of B's N columns at the same shared-memory address (the leader the
+// first half). The accumulate flag is an immediate.
 template <bool kAccumulate>
-__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                        uint32_t idesc) {
+__device__ __forceinline__ void umma_pair_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc) {
   if constexpr (kAccumulate)
-    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 1;" ::"r"(d_tmem),
+    asm volatile("tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, 1;" ::"r"(d_tmem),
                  "l"(a_desc), "l"(b_desc), "r"(idesc)
                  : "memory");
   else
-    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 0;" ::"r"(d_tmem),
+    asm volatile("tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, 0;" ::"r"(d_tmem),
                  "l"(a_desc), "l"(b_desc), "r"(idesc)
                  : "memory");
 }
 
+// The same with A read from tensor memory (M rows = lanes, each 32-bit column holding two
+// consecutive bf16 of K).
 template <bool kAccumulate>
-__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                        uint32_t idesc) {
+__device__ __forceinline__ void umma_pair_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc) {
   if constexpr (kAccumulate)
-    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, 1;" ::"r"(d_tmem),
+    asm volatile("tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, 1;" ::"r"(d_tmem),
                  "r"(a_tmem), "l"(b_desc), "r"(idesc)
                  : "memory");
   else
-    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, 0;" ::"r"(d_tmem),
+    asm volatile("tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, 0;" ::"r"(d_tmem),
                  "r"(a_tmem), "l"(b_desc), "r"(idesc)
                  : "memory");
 }
 
-// Arrive (once) on `bar` when every UMMA this thread issued so far has completed.
-__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+// Arrive (once) on the mbarrier at shared::cluster address `bar` -- in either CTA of the
+// pair -- when every UMMA this thread issued so far has completed.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar_cluster_addr) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_addr(bar))
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          bar_cluster_addr)
       : "memory");
 }
 
@@ -175,6 +162,38 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Two threads per TMEM lane: 16 consecutive lanes from taddr's lane; threads 0-15 receive
+// lane (base + i) at columns [col, col + 32), threads 16-31 lane (base + i - 16) at columns
+// [col + kSplit, col + kSplit + 32).
+template <int kSplit>
+__device__ __forceinline__ void tmem_ld16x2_32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32], %33;"
+      : PKV_R8(0), PKV_R8(8), PKV_R8(16), PKV_R8(24)
+      : "r"(taddr), "n"(kSplit));
+}
+
+template <int kSplit>
+__device__ __forceinline__ void tmem_st16x2_32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x32bx2.x32.b32 [%0], %1, "
+      "{%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"
+      "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33};" ::"r"(taddr),
+      "n"(kSplit), PKV_W8(0), PKV_W8(8), PKV_W8(16), PKV_W8(24)
+      : "memory");
+}
+
+template <int kSplit>
+__device__ __forceinline__ void tmem_st16x2_16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x32bx2.x16.b32 [%0], %1, "
+      "{%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17};" ::"r"(taddr),
+      "n"(kSplit), PKV_W8(0), PKV_W8(8)
+      : "memory");
 }
 
 #undef PKV_R8
