@@ -135,6 +135,10 @@ __global__ void __maxnreg__(96)
     }
     fence_mbar_init();
   }
+  // Launched as a programmatic dependent of the stream's previous kernel: everything above
+  // (barrier set-up) may overlap its tail; wait for that grid's completion and memory before
+  // touching global memory.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (__syncthreads_or(threadIdx.x == 0 && aborted(p.err))) return;  // uniform across the CTA
   // the merge kernel that follows may be scheduled now: it waits for this grid's completion
   // (and its memory) before reading anything
@@ -490,6 +494,9 @@ __global__ void __launch_bounds__(128)
                           const int32_t *__restrict__ context_lens, int32_t batch,
                           int32_t num_q_heads, int32_t chunk, int32_t splits, int64_t cap,
                           uint16_t *__restrict__ out) {
+  // the stream's next kernel (the next call's split kernel) may be scheduled now: it waits
+  // for this grid's completion before it touches global memory
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // launched as a programmatic dependent of the split kernel: wait until that grid has
   // completed and its partial results are visible
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -543,8 +550,19 @@ cudaError_t launch_split(const CUtensorMap &km, const CUtensorMap &vm, const Dec
     configured[dev] = true;
   }
   const int64_t ctas = std::min<int64_t>((int64_t)num_sms * 2, prm.units);
-  decode_split_kernel<GC><<<(unsigned)ctas, kThreads, smem, stream>>>(km, vm, prm);
-  return cudaGetLastError();
+  // a programmatic dependent of the stream's previous kernel: its launch and barrier set-up
+  // overlap that kernel's tail (it waits for the grid before reading anything)
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_split_kernel<GC>, km, vm, prm);
 }
 
 }  // namespace
