@@ -25,8 +25,11 @@
 //                  PV:  16 lanes per token (8 dims each), two tokens per instruction,
 //                       packed fp32x2 FMAs;
 //                at the end of a unit the 8 warp states are merged through shared memory.
-// With one split a unit writes bf16 output; otherwise it writes its normalised partial
-// output and log2-sum-exp, and decode_combine_kernel merges the splits.
+// With one split a unit writes bf16 output. With 2..8 splits and a static grid (one CTA per
+// unit, units ordered split-minor), the splits of one (sequence, head group) form a
+// thread-block cluster: each CTA leaves its normalised partial output and log2-sum-exp in its
+// own shared memory and the cluster's rank 0 merges them through distributed shared memory.
+// Otherwise a unit writes its partial to global memory and decode_combine_kernel merges.
 //
 // Algorithmic HBM bytes per (sequence, KV head, token): 256 (K) + 256 (V).
 #include <math.h>
@@ -44,6 +47,7 @@ constexpr int kTile = 64;
 constexpr int kConsumerWarps = 8;
 constexpr int kStages = 3;
 constexpr int kRing = 4;
+constexpr int kMaxCluster = 8;  // largest portable thread-block cluster
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kTileBytes = kTile * kD * 2;  // one head's K (or V) for 64 tokens: 16 KiB
 constexpr float kLog2e = 1.4426950408889634f;
@@ -64,6 +68,8 @@ struct DecodeSmem {
   uint16_t qs[kRing][GC][kD];  // q rows of the queued units
   alignas(16) uint16_t newkv[kRing][2][kD];  // a unit's new K and V rows, bound for the pool
   Unit unit[kRing];
+  float cl_o[GC][kD];  // cluster merge: this CTA's normalised output and log2-sum-exp
+  float cl_lse[GC];
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t unit_full[kRing];
@@ -87,6 +93,9 @@ struct DecodeParams {
   float *part_lse;
   uint16_t *out;
   int32_t *queue;  // next unit to hand out; nullptr: CTA i takes unit i only
+  // > 0: the splits of one (sequence, head group) form a cluster of this many CTAs (CTA i
+  // takes unit i, ordered split-minor); rank 0 merges them through distributed shared memory
+  int32_t cluster;
   unsigned int *err;
   int64_t num_blocks;
   int64_t cap;  // longest context the table rows and the split grid can address
@@ -123,6 +132,7 @@ __global__ void __maxnreg__(96)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  if (threadIdx.x < GC) sm.cl_lse[threadIdx.x] = -INFINITY;  // no result yet
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&sm.full[i], 1);
@@ -139,14 +149,17 @@ __global__ void __maxnreg__(96)
   // (barrier set-up) may overlap its tail; wait for that grid's completion and memory before
   // touching global memory.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (__syncthreads_or(threadIdx.x == 0 && aborted(p.err))) return;  // uniform across the CTA
+  // an earlier wait gave up somewhere (uniform across the CTA): return, or in a cluster do no
+  // work but still take part in the cluster's barriers
+  const bool stop = __syncthreads_or(threadIdx.x == 0 && aborted(p.err));
+  if (stop && !p.cluster) return;
   // the merge kernel that follows may be scheduled now: it waits for this grid's completion
   // (and its memory) before reading anything
   if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------------ producer
-    if (lane != 0) return;
+    if (lane == 0) {
     prefetch_tensormap(&kmap);
     prefetch_tensormap(&vmap);
     const uint64_t policy = policy_evict_first();
@@ -159,7 +172,8 @@ __global__ void __maxnreg__(96)
     while (ok) {
       // next unit with work (or one that must write zeros); ntiles < 0 ends the walk
       Unit un{0, 0, 0, -1, 0};
-      while (true) {
+      int32_t first_blk = -1;  // block id of the unit's first tile
+      while (!stop) {
         int u;
         if (p.queue) {
           u = atomicAdd(p.queue, 1);
@@ -168,15 +182,32 @@ __global__ void __maxnreg__(96)
           static_next = p.units;
         }
         if (u >= p.units) break;
-        const int s = u / (p.batch * p.xgroups);
-        const int r = u % (p.batch * p.xgroups);
-        const int b = r / p.xgroups, xg = r % p.xgroups;
-        int64_t L = p.context_lens[b];
+        int s, b, xg;
+        if (p.cluster) {  // split-minor: the splits of one (sequence, head group) adjacent
+          s = u % p.splits;
+          b = (u / p.splits) / p.xgroups;
+          xg = (u / p.splits) % p.xgroups;
+        } else {  // split-major
+          s = u / (p.batch * p.xgroups);
+          const int r = u % (p.batch * p.xgroups);
+          b = r / p.xgroups;
+          xg = r % p.xgroups;
+        }
+        // the first tile's block id does not depend on the context length: both loads are in
+        // flight together (a unit that starts past the table's end reads no entry)
+        const int64_t begin = (int64_t)s * p.chunk;
+        int64_t L;
+        if (begin < p.cap) {
+          L = ld_global_s32(p.context_lens + b);
+          first_blk = ld_global_s32(p.block_tables + (int64_t)b * p.table_width +
+                                    begin / p.block_size);
+        } else {
+          L = ld_global_s32(p.context_lens + b);
+        }
         if (L < 0 || L > p.cap) {
           if (s == 0 && xg == 0) record_error(p.err, 4u /* CONTEXT_RANGE */);
           L = L < 0 ? 0 : p.cap;
         }
-        const int64_t begin = (int64_t)s * p.chunk;
         if (begin < L) {
           const int64_t end = min(L, begin + p.chunk);
           // the unit that reads position L - 1 stores the new token there first (only one
@@ -185,7 +216,9 @@ __global__ void __maxnreg__(96)
                     p.k_new != nullptr && end == L ? 1 : 0};
           break;
         }
-        if (L == 0 && s == 0 && p.splits == 1) {  // empty context, direct output: zeros
+        if (p.cluster || (L == 0 && s == 0 && p.splits == 1)) {
+          // nothing to read: zeros (empty context), or in a cluster no result (the unit
+          // still leaves its -inf log2-sum-exp for the merge)
           un = Unit{b, s, xg, 0, 0};
           break;
         }
@@ -250,7 +283,7 @@ __global__ void __maxnreg__(96)
           bulk_wait_all();
         }
         const int pos = tok_begin + it * kTile;
-        const int64_t blk = table[pos / p.block_size];
+        const int64_t blk = it == 0 ? first_blk : table[pos / p.block_size];
         int32_t row;
         if (blk < 0 || blk >= p.num_blocks) {
           record_error(p.err, 2u /* BLOCK_RANGE */);
@@ -271,8 +304,10 @@ __global__ void __maxnreg__(96)
       drained = wait_own(&sm.full[t % kStages], (t / kStages) & 1, p.err);
     for (uint32_t k = pushed > kRing ? pushed - kRing : 0; drained && k < pushed; ++k)
       drained = wait_own(&sm.unit_full[k % kRing], (k / kRing) & 1, p.err);
-    return;
-  }
+    }
+    if (!p.cluster) return;
+    __syncwarp();
+  } else {
 
   // -------------------------------------------------------------------- consumers
   // QK: 4 lanes per token. Lane = (tq & 3) + 4 sub + 16 (tq >> 2): token tq of the warp's 8,
@@ -476,7 +511,10 @@ __global__ void __maxnreg__(96)
         lse = M + log2f(lsum);
       }
       const int64_t row = (int64_t)un.b * p.num_q_heads + hq0 + g;
-      if (p.splits == 1) {
+      if (p.cluster) {  // merged by the cluster's rank 0 at the end
+        sm.cl_o[g][d] = o;
+        if (d == 0) sm.cl_lse[g] = lse;  // -inf when the unit had no keys
+      } else if (p.splits == 1) {
         p.out[row * kD + d] = bf16_bits_rn(o);
       } else {
         p.part_o[(row * p.splits + un.s) * kD + d] = o;
@@ -485,6 +523,49 @@ __global__ void __maxnreg__(96)
     }
     named_barrier_sync(2, kConsumerWarps * 32);  // merge buffer free for the next unit
   }
+  }
+  if (!p.cluster) return;
+  // ---------------------------------------------------------------- cluster merge
+  // Every CTA of the cluster (one per split of this sequence and head group) has its result
+  // in shared memory; rank 0 reads them through distributed shared memory and writes the
+  // output, the others stay until it has read theirs.
+  cluster_sync();
+  if (cluster_ctarank() == 0 && threadIdx.x < GC * kD) {
+    const int g = threadIdx.x / kD, d = threadIdx.x % kD;
+    // all loads first (one round trip), then release the peers
+    const uint32_t lse_a = smem_addr(&sm.cl_lse[g]), o_a = smem_addr(&sm.cl_o[g][d]);
+    float l[kMaxCluster], o[kMaxCluster];
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r) {
+      l[r] = -INFINITY;
+      o[r] = 0.f;
+      if (r < p.splits) {
+        l[r] = ld_cluster_f32(cluster_addr(lse_a, r));
+        o[r] = ld_cluster_f32(cluster_addr(o_a, r));
+      }
+    }
+    cluster_arrive();  // the peers' shared memory is no longer needed
+    float M = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r) M = fmaxf(M, l[r]);
+    float acc = 0.f, wsum = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r) {
+        const float wgt = fast_exp2(l[r] - M);  // 0 for a split with no keys (and r >= splits)
+        wsum += wgt;
+        acc = fmaf(wgt, o[r], acc);
+      }
+    }
+    const int unit0 = blockIdx.x;  // rank 0 holds split 0
+    const int b = (unit0 / p.splits) / p.xgroups, xg = (unit0 / p.splits) % p.xgroups;
+    const int h = xg / p.head_groups;
+    const int64_t row = (int64_t)b * p.num_q_heads + h * p.group + (xg % p.head_groups) * GC + g;
+    if (!stop) p.out[row * kD + d] = bf16_bits_rn(wsum > 0.f ? acc / wsum : 0.f);
+  } else {
+    cluster_arrive();
+  }
+  cluster_wait();
 }
 
 // One warp per (sequence, query head): out = sum_s 2^(lse_s - lse) o_s over the sequence's
@@ -557,11 +638,18 @@ cudaError_t launch_split(const CUtensorMap &km, const CUtensorMap &vm, const Dec
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (prm.cluster) {  // one CTA per unit, the splits of a (sequence, head group) in a cluster
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)prm.cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
   return cudaLaunchKernelEx(&cfg, decode_split_kernel<GC>, km, vm, prm);
 }
 
@@ -663,15 +751,18 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &p, cudaSt
   }
 
   // With no more units than CTAs each CTA takes unit blockIdx.x and the counter (and the
-  // memset that resets it) is not needed.
+  // memset that resets it) is not needed. Then, with 2 to kMaxCluster splits, the splits of
+  // one (sequence, head group) run as one thread-block cluster and merge in distributed
+  // shared memory: no partials in global memory and no merge kernel.
   const bool queued = (int64_t)a.num_sms * 2 < units;
   cudaError_t e = cudaSuccess;
   if (queued) e = cudaMemsetAsync(prm.queue, 0, sizeof(int32_t), stream);
   else prm.queue = nullptr;
   if (e != cudaSuccess) return e;
+  prm.cluster = !queued && p.splits >= 2 && p.splits <= kMaxCluster ? p.splits : 0;
   e = p.heads_per_cta == 2 ? launch_split<2>(km, vm, prm, a.num_sms, stream)
                            : launch_split<1>(km, vm, prm, a.num_sms, stream);
-  if (e != cudaSuccess || p.splits == 1) return e;
+  if (e != cudaSuccess || p.splits == 1 || prm.cluster) return e;
   const int64_t rows_out = (int64_t)a.batch * a.num_q_heads;
   // programmatic dependent launch: the merge grid is set up while the split kernel runs
   cudaLaunchConfig_t cfg{};

@@ -123,6 +123,14 @@ __device__ __forceinline__ void cluster_sync() {
                    : "memory");
 }
 
+// The two halves of cluster_sync, for work between them (every thread of a warp together).
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Arrive on an mbarrier given by its shared::cluster address (this CTA's or another's), with
 // release semantics at cluster scope.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr) {
@@ -138,6 +146,12 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr) {
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster_addr) {
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr)
                : "memory");
+}
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t cluster_addr_) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr_) : "memory");
+  return v;
 }
 
 __device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr_, uint4 v) {
@@ -266,6 +280,14 @@ __device__ __forceinline__ bool barrier_or(uint32_t id, uint32_t threads, bool p
       : "r"((uint32_t)pred), "r"(id), "r"(threads)
       : "memory");
   return r != 0;
+}
+
+// A plain 32-bit global load kept in program order with the other volatile asm (so two
+// independent loads are both in flight before either value is used).
+__device__ __forceinline__ int32_t ld_global_s32(const int32_t *ptr) {
+  int32_t v;
+  asm volatile("ld.global.s32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {

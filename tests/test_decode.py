@@ -60,7 +60,7 @@ def test_decode_tiny_step(num_splits):
     (12, [255, 256, 257, 511, 512, 513, 1000, 1500]),
     (13, [3000, 17, 4097, 700]),
 ])
-@pytest.mark.parametrize("num_splits", [0, 1, 4])
+@pytest.mark.parametrize("num_splits", [0, 1, 4, 8, 9])
 def test_decode_ragged_contexts(seed, ctx, num_splits):
     lay, val = _host_case(ctx, seed=seed)
     ref = _oracle_step(lay, val)
