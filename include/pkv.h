@@ -78,6 +78,15 @@ int32_t pkv_abi_version(void);
 pkv_status pkv_get_device_errors(uint32_t *errors, int32_t reset);
 
 /*
+ * OR `bits` (PKV_DEVERR_* values) into the device-side error word of the current device.
+ * Setting PKV_DEVERR_TIMEOUT makes every later kernel of the library return without
+ * computing, exactly as after a wait that gave up; this is how the abort path is exercised
+ * without stalling anything. Synchronises the current device first. Returns
+ * PKV_ERR_CUDA if the device cannot be reached.
+ */
+pkv_status pkv_raise_device_errors(uint32_t bits);
+
+/*
  * kv_store -- the Triton store_kvcache of nano-vLLM («nano-vLLM 最小化vLLM重新实现»,
  * 架构 5: "writes K/V into the paged cache using slot_mapping, no Python loop").
  *

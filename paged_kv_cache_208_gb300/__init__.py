@@ -30,6 +30,7 @@ SIGNATURES = {
     "pkv_status_string": (ctypes.c_char_p, [_I32]),
     "pkv_abi_version": (_I32, []),
     "pkv_get_device_errors": (_I32, [ctypes.POINTER(ctypes.c_uint32), _I32]),
+    "pkv_raise_device_errors": (_I32, [ctypes.c_uint32]),
     "pkv_kv_store": (_I32, [_P, _I64, _P, _I64, _P, _I64, _P, _P, _I64, _I32, _I32, _P]),
     "pkv_decode_workspace_bytes": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32]),
     "pkv_paged_decode_attn": (_I32, [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32,
@@ -113,6 +114,12 @@ def get_device_errors(reset: bool = True) -> int:
     v = ctypes.c_uint32(0)
     _check("pkv_get_device_errors", _LIB.pkv_get_device_errors(ctypes.byref(v), int(reset)))
     return int(v.value)
+
+
+def raise_device_errors(bits: int) -> None:
+    """OR PKV_DEVERR_* bits into the device error word (synchronises). DEVERR_TIMEOUT makes
+    every later kernel return without computing until get_device_errors(reset=True)."""
+    _check("pkv_raise_device_errors", _LIB.pkv_raise_device_errors(int(bits)))
 
 
 def kv_store(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,

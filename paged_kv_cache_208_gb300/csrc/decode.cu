@@ -68,6 +68,8 @@ struct DecodeSmem {
   uint16_t qs[kRing][GC][kD];  // q rows of the queued units
   alignas(16) uint16_t newkv[kRing][2][kD];  // a unit's new K and V rows, bound for the pool
   Unit unit[kRing];
+  alignas(16) uint32_t zero16[4];  // an all-zero ldmatrix row (q rows past GC)
+  int32_t stop;  // set by the producer: an earlier wait gave up, this CTA does no work
   float cl_o[GC][kD];  // cluster merge: this CTA's normalised output and log2-sum-exp
   float cl_lse[GC];
   uint64_t full[kStages];
@@ -78,11 +80,12 @@ struct DecodeSmem {
 };
 
 // Byte offset of 16-byte chunk j (dims 8j..8j+7) of token t inside a swizzled tile. The TMA
-// box is {64 dims, 2 halves, 64 tokens}: 128-byte row r = 2t + (j >= 8), and the 128-byte
-// swizzle XORs the chunk index within the row with r mod 8.
+// box is {64 dims, 64 tokens, 2 halves}: half j / 8 of every token in its own 8 KiB plane of
+// 128-byte rows (row t), and the 128-byte swizzle XORs the chunk index within the row with
+// t mod 8, so the 8 rows of one ldmatrix (8 consecutive tokens, one chunk) hit 8 distinct
+// bank groups.
 __device__ __forceinline__ uint32_t tile_offset(int t, int j) {
-  const int r = 2 * t + (j >> 3);
-  return (uint32_t)((r << 7) | (((j & 7) ^ (r & 7)) << 4));
+  return (uint32_t)(((j >> 3) << 13) | (t << 7) | (((j & 7) ^ (t & 7)) << 4));
 }
 
 struct DecodeParams {
@@ -121,6 +124,22 @@ struct DecodeParams {
   int32_t num_kv_heads;
 };
 
+// Unit u -> (split s, sequence b, head group xg). A cluster launch orders the units
+// split-minor (the splits of one sequence and head group adjacent), otherwise split-major.
+__device__ __forceinline__ void unit_coords(const DecodeParams &p, int u, int &s, int &b,
+                                            int &xg) {
+  if (p.cluster) {
+    s = u % p.splits;
+    b = (u / p.splits) / p.xgroups;
+    xg = (u / p.splits) % p.xgroups;
+  } else {
+    s = u / (p.batch * p.xgroups);
+    const int r = u % (p.batch * p.xgroups);
+    b = r / p.xgroups;
+    xg = r % p.xgroups;
+  }
+}
+
 template <int GC>
 // 96 registers: warps are placed on the 4 SM sub-partitions (16K registers each), so two
 // 9-warp CTAs (5 warps on some sub-partitions) fit only at <= 102 registers per thread.
@@ -133,7 +152,9 @@ __global__ void __maxnreg__(96)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   if (threadIdx.x < GC) sm.cl_lse[threadIdx.x] = -INFINITY;  // no result yet
+  if (threadIdx.x < 4) sm.zero16[threadIdx.x] = 0u;
   if (threadIdx.x == 0) {
+    sm.stop = 0;
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&sm.full[i], 1);
       mbar_init(&sm.empty[i], kConsumerWarps);
@@ -145,14 +166,39 @@ __global__ void __maxnreg__(96)
     }
     fence_mbar_init();
   }
+  __syncthreads();
   // Launched as a programmatic dependent of the stream's previous kernel: everything above
   // (barrier set-up) may overlap its tail; wait for that grid's completion and memory before
   // touching global memory.
+  if (threadIdx.x == kConsumerWarps * 32) {
+    prefetch_tensormap(&kmap);
+    prefetch_tensormap(&vmap);
+  }
+  if (!p.queue && threadIdx.x == kConsumerWarps * 32) {
+    // Static grid: this CTA's unit is known now. While the previous grid finishes, warm L2
+    // with its context length, and with its first tiles through a block id read ahead of the
+    // wait. That read may see an old table (it is only a hint: L2 only, nothing kept in L1,
+    // and every value used below is read again after the wait).
+    int s, b, xg;
+    unit_coords(p, blockIdx.x, s, b, xg);
+    prefetch_l2(p.context_lens + b);
+    const int64_t begin = (int64_t)s * p.chunk;
+    if (begin < p.cap) {
+      const int32_t blk =
+          ld_global_cg_s32(p.block_tables + (int64_t)b * p.table_width + begin / p.block_size);
+      if (blk >= 0 && blk < p.num_blocks) {
+        const int in_block = (int)(begin % p.block_size);
+        const int n = min(kStages, min(p.chunk, p.block_size - in_block) / kTile);
+        const int h = xg / p.head_groups;
+        for (int t = 0; t < n; ++t) {
+          const int32_t row = (int32_t)((int64_t)blk * p.block_size + in_block + t * kTile);
+          tma_prefetch_3d(&kmap, 0, row, 2 * h);
+          tma_prefetch_3d(&vmap, 0, row, 2 * h);
+        }
+      }
+    }
+  }
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  // an earlier wait gave up somewhere (uniform across the CTA): return, or in a cluster do no
-  // work but still take part in the cluster's barriers
-  const bool stop = __syncthreads_or(threadIdx.x == 0 && aborted(p.err));
-  if (stop && !p.cluster) return;
   // the merge kernel that follows may be scheduled now: it waits for this grid's completion
   // (and its memory) before reading anything
   if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -160,8 +206,6 @@ __global__ void __maxnreg__(96)
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------------ producer
     if (lane == 0) {
-    prefetch_tensormap(&kmap);
-    prefetch_tensormap(&vmap);
     const uint64_t policy = policy_evict_first();
     uint32_t pushed = 0, tiles = 0;
     bool ok = true;
@@ -169,11 +213,12 @@ __global__ void __maxnreg__(96)
     uint32_t newkv_par = 0;        // bit s: parity of newkv_full[s]'s next phase
     bool newkv_pending = false;    // new-token rows on their way into shared memory
     int newkv_slot = 0;
+    bool first_unit = true;  // the abort bit is read with the first unit's loads
     while (ok) {
       // next unit with work (or one that must write zeros); ntiles < 0 ends the walk
       Unit un{0, 0, 0, -1, 0};
       int32_t first_blk = -1;  // block id of the unit's first tile
-      while (!stop) {
+      while (true) {
         int u;
         if (p.queue) {
           u = atomicAdd(p.queue, 1);
@@ -183,19 +228,14 @@ __global__ void __maxnreg__(96)
         }
         if (u >= p.units) break;
         int s, b, xg;
-        if (p.cluster) {  // split-minor: the splits of one (sequence, head group) adjacent
-          s = u % p.splits;
-          b = (u / p.splits) / p.xgroups;
-          xg = (u / p.splits) % p.xgroups;
-        } else {  // split-major
-          s = u / (p.batch * p.xgroups);
-          const int r = u % (p.batch * p.xgroups);
-          b = r / p.xgroups;
-          xg = r % p.xgroups;
-        }
+        unit_coords(p, u, s, b, xg);
         // the first tile's block id does not depend on the context length: both loads are in
         // flight together (a unit that starts past the table's end reads no entry)
         const int64_t begin = (int64_t)s * p.chunk;
+        // an earlier wait gave up somewhere: end the walk (in a cluster the CTA still takes
+        // part in the cluster's barriers)
+        const uint32_t err_now =
+            first_unit && p.err ? (uint32_t)ld_global_s32(reinterpret_cast<const int32_t *>(p.err)) : 0u;
         int64_t L;
         if (begin < p.cap) {
           L = ld_global_s32(p.context_lens + b);
@@ -203,6 +243,13 @@ __global__ void __maxnreg__(96)
                                     begin / p.block_size);
         } else {
           L = ld_global_s32(p.context_lens + b);
+        }
+        if (first_unit) {
+          first_unit = false;
+          if (err_now & kErrTimeout) {
+            sm.stop = 1;
+            break;
+          }
         }
         if (L < 0 || L > p.cap) {
           if (s == 0 && xg == 0) record_error(p.err, 4u /* CONTEXT_RANGE */);
@@ -292,8 +339,8 @@ __global__ void __maxnreg__(96)
           row = (int32_t)(blk * p.block_size + pos % p.block_size);
         }
         mbar_arrive_expect_tx(&sm.full[stage], 2 * kTileBytes);
-        tma_load_3d(sm.k[stage], &kmap, &sm.full[stage], 0, 2 * h, row, policy);
-        tma_load_3d(sm.v[stage], &vmap, &sm.full[stage], 0, 2 * h, row, policy);
+        tma_load_3d(sm.k[stage], &kmap, &sm.full[stage], 0, row, 2 * h, policy);
+        tma_load_3d(sm.v[stage], &vmap, &sm.full[stage], 0, row, 2 * h, policy);
       }
     }
     // keep the CTA alive until every copy it issued has landed (also after an abort: these
@@ -310,21 +357,24 @@ __global__ void __maxnreg__(96)
   } else {
 
   // -------------------------------------------------------------------- consumers
-  // QK: 4 lanes per token. Lane = (tq & 3) + 4 sub + 16 (tq >> 2): token tq of the warp's 8,
-  // sub selects chunks {r, r+8, r+4, r+12}[sub] for r = 0..3. A quarter-warp (8 lanes, one
-  // 128-bit shared-memory phase) then reads 4 tokens x chunks {c, c + 8}, which sit in
-  // different swizzle rows, so its 8 accesses hit 8 distinct bank groups.
-  const int tq = (lane & 3) | ((lane >> 4) << 2);
-  const int sub = (lane >> 2) & 3;
-  const int hw = lane >> 4;   // PV: token parity
-  const int dl = lane & 15;   // PV: chunk (dims 8dl..8dl+7)
-  const int t_qk = warp * 8 + tq;
-  const int chunk0 = 8 * (sub & 1) + 4 * (sub >> 1);  // chunks chunk0 + r, r = 0..3
-  uint32_t off_qk[4], off_pv[4];
+  // Warp w owns tokens [8w, 8w + 8) of every 64-token tile; both products run as warp-level
+  // MMAs with the unit's query heads as the M rows (GC of 16 used):
+  //   S   (16 heads x 8 tokens) = Q (16 x 128) K^T        m16n8k16, 8 steps over the dims
+  //   O^T (16 dims x 8 heads)  += V^T (16 x 8 tokens) P^T  m16n8k8, 8 blocks of 16 dims
+  // Lane l = 4 gq + tq holds S for head gq and tokens 2tq, 2tq + 1, which is exactly its
+  // share of the P^T operand of the second product: P stays in registers (rounded to bf16,
+  // and l sums the rounded values). Its O^T accumulator holds heads 2tq and 2tq + 1.
+  const int gq = lane >> 2, tq = lane & 3;
+  const int tok = warp * 8 + 2 * tq;  // tile-relative token of S column 2tq
+  // ldmatrix row addresses: lanes 8i..8i+7 give matrix i of load j = dims chunk 4j + i of
+  // tokens 8w..8w+7
+  uint32_t off_ld[4];
 #pragma unroll
-  for (int r = 0; r < 4; ++r) off_qk[r] = tile_offset(t_qk, chunk0 + r);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) off_pv[i] = tile_offset(warp * 8 + 2 * i + hw, dl);
+  for (int j = 0; j < 4; ++j) off_ld[j] = tile_offset(warp * 8 + (lane & 7), 4 * j + (lane >> 3));
+  const uint32_t k_base = smem_addr(sm.k[0]), v_base = smem_addr(sm.v[0]);
+  // q: ldmatrix row (lane & 7) = head, matrix (lane >> 3) = dims chunk; heads past GC read zeros
+  const bool q_row = (lane & 7) < GC;
+  const uint32_t q_zero = smem_addr(sm.zero16);
 
   // Every decision to leave the unit loop is taken by all 8 consumer warps together (a
   // barrier reduction), so no warp can be left waiting in a merge barrier.
@@ -338,157 +388,114 @@ __global__ void __maxnreg__(96)
     if (un.ntiles < 0) break;
     const int h = un.xg / p.head_groups;
     const int hq0 = h * p.group + (un.xg % p.head_groups) * GC;
-    // q stays packed bf16: QK uses mixed-precision FMAs, the scale is applied to the score
-    uint32_t qw[GC][4][4];
-#pragma unroll
-    for (int g = 0; g < GC; ++g)
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const uint4 w4 = *reinterpret_cast<const uint4 *>(&sm.qs[slot][g][8 * (chunk0 + r)]);
-        qw[g][r][0] = w4.x;
-        qw[g][r][1] = w4.y;
-        qw[g][r][2] = w4.z;
-        qw[g][r][3] = w4.w;
-      }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.unit_empty[slot]);
+    // q's A fragments are read again for every tile (ldmatrix, cheaper than holding them in
+    // registers): the ring slot stays taken until the unit ends
+    const uint32_t q_base =
+        q_row ? smem_addr(&sm.qs[slot][lane & 7][8 * (lane >> 3)]) : q_zero;
+    const uint32_t q_step = q_row ? 64u : 0u;  // 4 chunks of 16 bytes per load
 
     int64_t L = p.context_lens[un.b];
     L = L < 0 ? 0 : (L > p.cap ? p.cap : L);
     const int tok_begin = un.s * p.chunk;
     const int tok_end = (int)min(L, (int64_t)tok_begin + p.chunk);
 
-    float m_run[GC], l_run[GC];
-    float2 acc[GC][4];  // dims 8dl + 2e, 8dl + 2e + 1
+    float m_run = -INFINITY;  // running maximum of head gq (the same in the lane's quad)
+    float l_run = 0.f;        // this lane's share of head gq's sum
+    float acc[8][4];          // O^T: dims 16m + gq (+8) x heads 2tq, 2tq + 1
 #pragma unroll
-    for (int g = 0; g < GC; ++g) {
-      m_run[g] = -INFINITY;
-      l_run[g] = 0.f;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[g][e] = make_float2(0.f, 0.f);
-    }
+    for (int m = 0; m < 8; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
 
     bool ok = true;
     for (int it = 0; it < un.ntiles; ++it, ++tiles) {
       const int stage = tiles % kStages;
-      // warp-uniform: the loop body uses full-warp shuffles
+      // warp-uniform: the loop body uses warp-wide MMAs and shuffles
       if (!__all_sync(kFull, wait_parity(&sm.full[stage], (tiles / kStages) & 1, p.err))) {
         ok = false;
         break;
       }
-      const uint8_t *kt = sm.k[stage];
-      const uint8_t *vt = sm.v[stage];
+      const uint32_t kt = k_base + stage * kTileBytes;
+      const uint32_t vt = v_base + stage * kTileBytes;
       const int n_valid = tok_end - (tok_begin + it * kTile);  // >= 1; < 64 only in a last tile
 
-      // ---- scores for token t_qk (log2 domain)
-      float sc[GC];
-      {
-        float s_lo[GC], s_hi[GC];
+      // ---- S = Q K^T for the warp's 8 tokens (two accumulators: half the dependency chain)
+      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int g = 0; g < GC; ++g) s_lo[g] = s_hi[g] = 0.f;
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const uint4 k4 = *reinterpret_cast<const uint4 *>(kt + off_qk[r]);
-          const uint32_t w[4] = {k4.x, k4.y, k4.z, k4.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-#pragma unroll
-            for (int g = 0; g < GC; ++g) fma_bf16_pairs(qw[g][r][e], w[e], s_lo[g], s_hi[g]);
-        }
-#pragma unroll
-        for (int g = 0; g < GC; ++g) {
-          float v = s_lo[g] + s_hi[g];
-          v += __shfl_xor_sync(kFull, v, 4);   // the 4 lanes of a token differ in lane bits 2-3
-          v += __shfl_xor_sync(kFull, v, 8);
-          sc[g] = v * p.qscale;
-        }
+      for (int j = 0; j < 4; ++j) {  // dims [32j, 32j + 32): two k-steps
+        uint32_t qf[4], kb[4];
+        ldsm_x4(q_base + j * q_step, qf);  // head rows: dims chunks 4j .. 4j + 3
+        ldsm_x4(kt + off_ld[j], kb);        // token rows: the same chunks
+        mma_bf16_16816(s0, qf[0], 0u, qf[1], 0u, kb[0], kb[1]);
+        mma_bf16_16816(s1, qf[2], 0u, qf[3], 0u, kb[2], kb[3]);
       }
+      uint32_t vb[16];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) ldsm_x4_trans(vt + off_ld[j], &vb[4 * j]);
+
+      // ---- online softmax (log2 domain); heads past GC and tokens past the context drop out
+      float sa = (s0[0] + s1[0]) * p.qscale;
+      float sb = (s0[1] + s1[1]) * p.qscale;
+      if (gq >= GC) sa = sb = -INFINITY;
       if (n_valid < kTile) {
+        if (tok >= n_valid) sa = -INFINITY;
+        if (tok + 1 >= n_valid) sb = -INFINITY;
+        // their V rows may hold anything (0 * NaN would poison the sums): zero them
+        const uint32_t vmask = (tok < n_valid ? 0x0000ffffu : 0u) | (tok + 1 < n_valid ? 0xffff0000u : 0u);
 #pragma unroll
-        for (int g = 0; g < GC; ++g)
-          if (t_qk >= n_valid) sc[g] = -INFINITY;
+        for (int c = 0; c < 16; ++c) vb[c] &= vmask;
       }
+      float mx = fmaxf(sa, sb);
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+      if (__any_sync(kFull, mx > m_run)) {
+        const float m_new = fmaxf(m_run, mx);
+        const float alpha = m_new == -INFINITY ? 1.f : fast_exp2(m_run - m_new);
+        l_run *= alpha;
+        m_run = m_new;
+        // the accumulator's heads 2tq and 2tq + 1 live in quads 2tq and 2tq + 1
+        const float a_lo = __shfl_sync(kFull, alpha, 8 * tq);
+        const float a_hi = __shfl_sync(kFull, alpha, 8 * tq + 4);
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          acc[m][0] *= a_lo;
+          acc[m][1] *= a_hi;
+          acc[m][2] *= a_lo;
+          acc[m][3] *= a_hi;
+        }
+      }
+      float pa = 0.f, pb = 0.f;
+      if (m_run != -INFINITY) {
+        pa = fast_exp2(sa - m_run);
+        pb = fast_exp2(sb - m_run);
+      }
+      const uint32_t pf = pack_bf16x2(pa, pb);
+      l_run += bf16_lo(pf) + bf16_hi(pf);
 
-      // ---- online softmax over the warp's 8 tokens
-      float pr[GC];
-      bool any = false;
+      // ---- O^T += V^T P^T
 #pragma unroll
-      for (int g = 0; g < GC; ++g) {
-        float mx = sc[g];  // the warp's 8 tokens differ in lane bits 0, 1 and 4
-        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
-        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
-        if (mx > m_run[g]) {  // warp-uniform: every lane holds the same maxima
-          const float alpha = fast_exp2(m_run[g] - mx);
-          l_run[g] *= alpha;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            acc[g][e].x *= alpha;
-            acc[g][e].y *= alpha;
-          }
-          m_run[g] = mx;
-        }
-        if (m_run[g] != -INFINITY) {
-          any = true;
-          pr[g] = fast_exp2(sc[g] - m_run[g]);
-          float ps = pr[g];
-          ps += __shfl_xor_sync(kFull, ps, 1);
-          ps += __shfl_xor_sync(kFull, ps, 2);
-          ps += __shfl_xor_sync(kFull, ps, 16);
-          l_run[g] += ps;
-        } else {
-          pr[g] = 0.f;
-        }
-      }
-
-      // ---- acc += p v, two tokens per instruction (half-warp hw takes token 2i + hw)
-      if (any) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int tt = 2 * i + hw;
-          float2 pv[GC];
-#pragma unroll
-          for (int g = 0; g < GC; ++g) {
-            const float x = __shfl_sync(kFull, pr[g], (tt & 3) | ((tt >> 2) << 4));
-            pv[g] = make_float2(x, x);
-          }
-          if (n_valid >= kTile || warp * 8 + tt < n_valid) {
-            const uint4 v4 = *reinterpret_cast<const uint4 *>(vt + off_pv[i]);
-            const uint32_t w[4] = {v4.x, v4.y, v4.z, v4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 vf = make_float2(bf16_lo(w[e]), bf16_hi(w[e]));
-#pragma unroll
-              for (int g = 0; g < GC; ++g) acc[g][e] = ffma2(pv[g], vf, acc[g][e]);
-            }
-          }
-        }
-      }
+      for (int m = 0; m < 8; ++m) mma_bf16_1688(acc[m], vb[2 * m], vb[2 * m + 1], pf);
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.empty[stage]);
     }
 
-    // ---- merge: half-warps, then the 8 warps through shared memory
-#pragma unroll
-    for (int g = 0; g < GC; ++g)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        acc[g][e].x += __shfl_xor_sync(kFull, acc[g][e].x, 16);
-        acc[g][e].y += __shfl_xor_sync(kFull, acc[g][e].y, 16);
-      }
-    if (lane < 16) {
-#pragma unroll
-      for (int g = 0; g < GC; ++g) {
-        float4 *dst = reinterpret_cast<float4 *>(&sm.acc[warp][g][8 * dl]);
-        dst[0] = make_float4(acc[g][0].x, acc[g][0].y, acc[g][1].x, acc[g][1].y);
-        dst[1] = make_float4(acc[g][2].x, acc[g][2].y, acc[g][3].x, acc[g][3].y);
-      }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.unit_empty[slot]);  // q no longer needed
+
+    // ---- merge: the quad's shares of l, then the 8 warps through shared memory
+    l_run += __shfl_xor_sync(kFull, l_run, 1);
+    l_run += __shfl_xor_sync(kFull, l_run, 2);
+    if (tq == 0 && gq < GC) {
+      sm.m[warp][gq] = m_run;
+      sm.l[warp][gq] = l_run;
     }
-    if (lane == 0) {
 #pragma unroll
-      for (int g = 0; g < GC; ++g) {
-        sm.m[warp][g] = m_run[g];
-        sm.l[warp][g] = l_run[g];
+    for (int e = 0; e < 2; ++e) {
+      const int hh = 2 * tq + e;
+      if (hh < GC) {
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          sm.acc[warp][hh][16 * m + gq] = acc[m][e];
+          sm.acc[warp][hh][16 * m + gq + 8] = acc[m][2 + e];
+        }
       }
     }
     if (barrier_or(1, kConsumerWarps * 32, !ok)) break;  // a wait gave up: stop together
@@ -561,7 +568,7 @@ __global__ void __maxnreg__(96)
     const int b = (unit0 / p.splits) / p.xgroups, xg = (unit0 / p.splits) % p.xgroups;
     const int h = xg / p.head_groups;
     const int64_t row = (int64_t)b * p.num_q_heads + h * p.group + (xg % p.head_groups) * GC + g;
-    if (!stop) p.out[row * kD + d] = bf16_bits_rn(wsum > 0.f ? acc / wsum : 0.f);
+    if (!sm.stop) p.out[row * kD + d] = bf16_bits_rn(wsum > 0.f ? acc / wsum : 0.f);
   } else {
     cluster_arrive();
   }
@@ -574,13 +581,14 @@ __global__ void __launch_bounds__(128)
     decode_combine_kernel(const float *__restrict__ part_o, const float *__restrict__ part_lse,
                           const int32_t *__restrict__ context_lens, int32_t batch,
                           int32_t num_q_heads, int32_t chunk, int32_t splits, int64_t cap,
-                          uint16_t *__restrict__ out) {
+                          uint16_t *__restrict__ out, const unsigned int *err) {
   // the stream's next kernel (the next call's split kernel) may be scheduled now: it waits
   // for this grid's completion before it touches global memory
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // launched as a programmatic dependent of the split kernel: wait until that grid has
   // completed and its partial results are visible
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (aborted(err)) return;  // an earlier wait gave up: the partials are not complete
   const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
   if (row >= (int64_t)batch * num_q_heads) return;
   const int lane = threadIdx.x & 31;
@@ -668,16 +676,16 @@ DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
     const int64_t per = (max_ctx + S - 1) / S;
     p.chunk = (int32_t)((per + kTile - 1) / kTile * kTile);
   } else {
-    // Each unit ends with a merge across the CTA's warps, so long units (up to 16 tiles) pay
-    // off, but one CTA streams a unit through a 3-tile ring, which caps its own bandwidth:
-    // enough units must run at once to fill HBM. Measured over batches 1..256 of 1024- and
-    // 2048-token contexts, the best choice is the longest chunk that still leaves about
-    // 1.5 units per SM (the work queue balances the rest).
-    // The split count is chosen first and the context divided evenly among the splits.
+    // At most 16 tiles per unit (a CTA streams its unit through a 3-tile ring, so long
+    // units cap the bandwidth of a skewed batch; the work queue balances short ones). Below
+    // that, more splits give more CTAs for a small batch, but every CTA past one per SM
+    // shares an SM, and a unit's fixed costs (its first tile's latency, the merges) do not
+    // shrink. Measured on batches 1..64 at 1024 tokens, the best split count is the largest
+    // that keeps the grid within about 1.7 CTAs per SM and its splits within one cluster.
     const int64_t units = (int64_t)batch * num_kv_heads * p.head_groups;
-    const int64_t target = (int64_t)num_sms * 3 / 2;
-    int64_t S = (max_tiles + 15) / 16;  // at most 16 tiles per unit
-    while (S < max_tiles && units * S < target) ++S;
+    const int64_t limit = (int64_t)num_sms * 17 / 10;
+    int64_t S = (max_tiles + 15) / 16;
+    while (S < max_tiles && S < kMaxCluster && units * (S + 1) <= limit) ++S;
     const int64_t per = (max_ctx + S - 1) / S;
     p.chunk = (int32_t)((per + kTile - 1) / kTile * kTile);
   }
@@ -689,12 +697,14 @@ DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
 }
 
 cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &p, cudaStream_t stream) {
-  // TMA views of the two pools: {64 dims, 2 * Hkv half-heads, num_blocks * block_size rows}
+  // TMA views of the two pools: {64 dims, num_blocks * block_size rows, 2 * Hkv half-heads}
+  // (the half-head stride, 128 bytes, is the innermost of the two): a tile lands as two
+  // planes, one per half of the head dimension
   CUtensorMap km, vm;
   const uint64_t rows = (uint64_t)a.num_blocks * a.block_size;
-  const uint64_t dims[3] = {64, (uint64_t)a.num_kv_heads * 2, rows};
-  const uint64_t strides[2] = {128, (uint64_t)a.num_kv_heads * kD * 2};
-  const uint32_t box[3] = {64, 2, kTile};
+  const uint64_t dims[3] = {64, rows, (uint64_t)a.num_kv_heads * 2};
+  const uint64_t strides[2] = {(uint64_t)a.num_kv_heads * kD * 2, 128};
+  const uint32_t box[3] = {64, kTile, 2};
   if (encode_tensor_map(&km, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(a.k_cache),
                         dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B) != CUDA_SUCCESS ||
@@ -777,7 +787,8 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &p, cudaSt
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, decode_combine_kernel, (const float *)prm.part_o,
                             (const float *)prm.part_lse, a.context_lens, a.batch, a.num_q_heads,
-                            p.chunk, p.splits, prm.cap, static_cast<uint16_t *>(a.out));
+                            p.chunk, p.splits, prm.cap, static_cast<uint16_t *>(a.out),
+                            (const unsigned int *)a.err);
 }
 
 }  // namespace pkv

@@ -116,6 +116,16 @@ const char *pkv_status_string(pkv_status status) {
 
 int32_t pkv_abi_version(void) { return 1; }
 
+pkv_status pkv_raise_device_errors(uint32_t bits) {
+  if (!device_info()) return PKV_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return PKV_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_errors, sizeof v) != cudaSuccess) return PKV_ERR_CUDA;
+  v |= bits;
+  if (cudaMemcpyToSymbol(g_device_errors, &v, sizeof v) != cudaSuccess) return PKV_ERR_CUDA;
+  return PKV_OK;
+}
+
 pkv_status pkv_get_device_errors(uint32_t *errors, int32_t reset) {
   if (!errors) return PKV_ERR_INVALID_ARG;
   if (!device_info()) return PKV_ERR_CUDA;

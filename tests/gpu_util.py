@@ -31,6 +31,7 @@ def assert_attention_close(got: torch.Tensor, ref: np.ndarray, what: str = "") -
     """max |got - ref| <= 1e-2 + 1e-2 |ref| element by element (bf16 in, fp32 accumulate)."""
     g = host_f64(got)
     assert g.shape == ref.shape, (g.shape, ref.shape)
+    assert np.isfinite(ref).all(), f"{what}: non-finite reference (inputs read unset slots?)"
     assert np.isfinite(g).all(), f"{what}: non-finite output"
     err = np.abs(g - ref)
     bound = TOL_ABS + TOL_REL * np.abs(ref)
