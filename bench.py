@@ -317,13 +317,11 @@ def time_prefill_store(pkv, iters: int = 20):
             "bytes": nbytes, "l2": "inputs (1.18 GB) larger than L2"}
 
 
-def time_decode_shape(pkv, batch: int, ctx: int, hbm_peak: float, iters: int = 20,
-                      graph: bool = False):
-    """Paged decode attention alone on `batch` sequences of `ctx` tokens (blocks drawn at
-    random). Small batches rotate over enough disjoint copies of the pool region that the
-    timed reads (>= 1 GB across the rotation) do not come from L2. With `graph`, one CUDA
-    graph holds one call per copy and is replayed, so the time is the GPU's alone (no host
-    call overhead between launches)."""
+def decode_shape_calls(pkv, batch: int, ctx: int):
+    """`batch` sequences of `ctx` tokens (blocks drawn at random). Small batches rotate over
+    enough disjoint copies of the pool region that the reads (>= 1 GB across the rotation)
+    do not come from L2. Returns (call, reps, tables, keep): call(r) runs paged decode on
+    copy r of reps; keep holds the device tensors alive."""
     per = batch * (-(-ctx // BS))
     reps = max(1, -(-(1 << 30) // (per * BS * ROW_BYTES * 2)))
     lay = w.decode_layout(np.full(batch * reps, ctx, np.int32), per * reps + 8, w.rng(5 + batch))
@@ -337,19 +335,34 @@ def time_decode_shape(pkv, batch: int, ctx: int, hbm_peak: float, iters: int = 2
     ws = pkv.decode_workspace(batch, HQ, HKV, D, ctx, 0)
     call = lambda r: pkv.paged_decode_attn(q, kc, vc, tables[r], cl, ctx, D ** -0.5,
                                            workspace=ws, out=out)
+    return call, reps, tables, (kc, vc, q, out, cl, ws)
+
+
+def capture_graph(call, reps: int):
+    """One CUDA graph holding call(0) .. call(reps - 1), back to back."""
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for r in range(reps):
+                call(r)
+    torch.cuda.current_stream().wait_stream(s)
+    return g
+
+
+def time_decode_shape(pkv, batch: int, ctx: int, hbm_peak: float, iters: int = 20,
+                      graph: bool = False):
+    """Paged decode attention alone on `batch` sequences of `ctx` tokens (decode_shape_calls).
+    With `graph`, one CUDA graph holds one call per pool copy and is replayed, so the time is
+    the GPU's alone (no host call overhead between launches)."""
+    call, reps, tables, keep = decode_shape_calls(pkv, batch, ctx)
     for r in range(min(reps, 3)):
         call(r)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if graph:
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        s = torch.cuda.Stream()
-        s.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(s):
-            with torch.cuda.graph(g, stream=s):
-                for r in range(reps):
-                    call(r)
-        torch.cuda.current_stream().wait_stream(s)
+        g = capture_graph(call, reps)
         replays = max(1, -(-iters // reps))
         for _ in range(2):
             g.replay()
@@ -370,7 +383,7 @@ def time_decode_shape(pkv, batch: int, ctx: int, hbm_peak: float, iters: int = 2
         n = iters
     t = e0.elapsed_time(e1) / 1e3 / n
     nbytes = decode_bytes(np.full(batch, ctx), tables[0].shape[1])["decode"]
-    del kc, vc
+    del keep
     return {"batch": batch, "ctx": ctx, "us": t * 1e6, "gbs": nbytes / t / 1e9,
             "frac_of_hbm_peak": nbytes / t / 1e9 / hbm_peak, "kv_tokens_per_s": batch * ctx / t,
             "timing": "cuda graph replay" if graph else "eager calls"}
@@ -736,7 +749,8 @@ def run_reference(args):
 
 def run_profile(args):
     """One kernel alone on its workload, for ncu: `decode` (the Qwen3 batch, one layer, a pool
-    of just the referenced blocks: 1.2 GB, larger than L2), `prefill` (the varlen workload,
+    of just the referenced blocks: 1.2 GB, larger than L2), `decode_small` (--profile-batch
+    sequences of 1024 tokens, graph-replayed), `decode_long` (8 x 32768), `prefill` (the varlen workload,
     packed), `prefix` (the prefix-cached workload, keys through block_table) or `store` (the
     varlen workload's kv_store). Runs --warmup + --steps launches."""
     torch.cuda.set_device(0)
@@ -750,6 +764,16 @@ def run_profile(args):
                                             s[0, 0], s[1, 0], step.tables, step.ctx, step.maxc,
                                             step.lay.scale, num_splits=args.num_splits,
                                             workspace=step.ws, out=step.out[0])
+    elif args.profile == "decode_small":
+        # --profile-batch sequences of 1024 tokens through the batch sweep's rotation of pool
+        # copies; one CUDA graph of one call per copy, replayed (--warmup + --steps) times
+        call, reps, _, keep = decode_shape_calls(pkv, args.profile_batch, 1024)
+        g = capture_graph(call, reps)
+        run = g.replay
+    elif args.profile == "decode_long":
+        # the long-context shape reduced to 8 sequences x 32768 tokens (1.07 GB of K+V)
+        call, reps, _, keep = decode_shape_calls(pkv, 8, 32768)
+        run = lambda: call(0)
     elif args.profile == "store":
         lens = w.varlen_prefill_lengths()
         lay = w.varlen_prefill_layout(num_blocks=w.blocks_needed(lens) + 64)
@@ -815,7 +839,10 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--num-splits", type=int, default=0,
                     help="decode KV splits of the longest context (0 = the library's choice)")
-    ap.add_argument("--profile", choices=["decode", "prefill", "prefix", "store", "rope"],
+    ap.add_argument("--profile-batch", type=int, default=8,
+                    help="sequences for --profile decode_small")
+    ap.add_argument("--profile", choices=["decode", "decode_small", "decode_long", "prefill",
+                                          "prefix", "store", "rope"],
                     help="run one kernel alone (for ncu); prints no benchmark line")
     args = ap.parse_args()
     if args.warmup < 3:

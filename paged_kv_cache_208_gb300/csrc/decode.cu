@@ -188,7 +188,7 @@ __global__ void __maxnreg__(96)
           ld_global_cg_s32(p.block_tables + (int64_t)b * p.table_width + begin / p.block_size);
       if (blk >= 0 && blk < p.num_blocks) {
         const int in_block = (int)(begin % p.block_size);
-        const int n = min(kStages, min(p.chunk, p.block_size - in_block) / kTile);
+        const int n = min(2 * kStages, min(p.chunk, p.block_size - in_block) / kTile);
         const int h = xg / p.head_groups;
         for (int t = 0; t < n; ++t) {
           const int32_t row = (int32_t)((int64_t)blk * p.block_size + in_block + t * kTile);
@@ -341,6 +341,7 @@ __global__ void __maxnreg__(96)
         mbar_arrive_expect_tx(&sm.full[stage], 2 * kTileBytes);
         tma_load_3d(sm.k[stage], &kmap, &sm.full[stage], 0, row, 2 * h, policy);
         tma_load_3d(sm.v[stage], &vmap, &sm.full[stage], 0, row, 2 * h, policy);
+
       }
     }
     // keep the CTA alive until every copy it issued has landed (also after an abort: these
@@ -388,11 +389,18 @@ __global__ void __maxnreg__(96)
     if (un.ntiles < 0) break;
     const int h = un.xg / p.head_groups;
     const int hq0 = h * p.group + (un.xg % p.head_groups) * GC;
-    // q's A fragments are read again for every tile (ldmatrix, cheaper than holding them in
-    // registers): the ring slot stays taken until the unit ends
-    const uint32_t q_base =
-        q_row ? smem_addr(&sm.qs[slot][lane & 7][8 * (lane >> 3)]) : q_zero;
-    const uint32_t q_step = q_row ? 64u : 0u;  // 4 chunks of 16 bytes per load
+    // q's A fragments, held in registers for the unit: load j gives dims [32j, 32j + 32) as
+    // a0, a2 of k-step 2j and a0, a2 of k-step 2j + 1 (rows 8-15, a1 and a3, are zero)
+    uint32_t qa[4][4];
+    {
+      const uint32_t q_base =
+          q_row ? smem_addr(&sm.qs[slot][lane & 7][8 * (lane >> 3)]) : q_zero;
+      const uint32_t q_step = q_row ? 64u : 0u;  // 4 chunks of 16 bytes per load
+#pragma unroll
+      for (int j = 0; j < 4; ++j) ldsm_x4(q_base + j * q_step, qa[j]);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.unit_empty[slot]);
 
     int64_t L = p.context_lens[un.b];
     L = L < 0 ? 0 : (L > p.cap ? p.cap : L);
@@ -421,11 +429,10 @@ __global__ void __maxnreg__(96)
       float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {  // dims [32j, 32j + 32): two k-steps
-        uint32_t qf[4], kb[4];
-        ldsm_x4(q_base + j * q_step, qf);  // head rows: dims chunks 4j .. 4j + 3
-        ldsm_x4(kt + off_ld[j], kb);        // token rows: the same chunks
-        mma_bf16_16816(s0, qf[0], 0u, qf[1], 0u, kb[0], kb[1]);
-        mma_bf16_16816(s1, qf[2], 0u, qf[3], 0u, kb[2], kb[3]);
+        uint32_t kb[4];
+        ldsm_x4(kt + off_ld[j], kb);  // token rows: dims chunks 4j .. 4j + 3
+        mma_bf16_16816(s0, qa[j][0], 0u, qa[j][1], 0u, kb[0], kb[1]);
+        mma_bf16_16816(s1, qa[j][2], 0u, qa[j][3], 0u, kb[2], kb[3]);
       }
       uint32_t vb[16];
 #pragma unroll
@@ -477,9 +484,6 @@ __global__ void __maxnreg__(96)
       if (lane == 0) mbar_arrive(&sm.empty[stage]);
     }
 
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.unit_empty[slot]);  // q no longer needed
-
     // ---- merge: the quad's shares of l, then the 8 warps through shared memory
     l_run += __shfl_xor_sync(kFull, l_run, 1);
     l_run += __shfl_xor_sync(kFull, l_run, 2);
@@ -528,6 +532,7 @@ __global__ void __maxnreg__(96)
         if (d == 0) p.part_lse[row * p.splits + un.s] = lse;
       }
     }
+    if (!p.queue) break;  // a static grid gives each CTA one unit: nothing follows
     named_barrier_sync(2, kConsumerWarps * 32);  // merge buffer free for the next unit
   }
   }
@@ -681,11 +686,14 @@ DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
     // that, more splits give more CTAs for a small batch, but every CTA past one per SM
     // shares an SM, and a unit's fixed costs (its first tile's latency, the merges) do not
     // shrink. Measured on batches 1..64 at 1024 tokens, the best split count is the largest
-    // that keeps the grid within about 1.7 CTAs per SM and its splits within one cluster.
+    // that keeps its splits within one cluster and the grid within about 1.7 CTAs per SM,
+    // or within one CTA per SM for clusters of more than 4 (larger clusters do not all fit
+    // at once when SMs hold two CTAs).
     const int64_t units = (int64_t)batch * num_kv_heads * p.head_groups;
-    const int64_t limit = (int64_t)num_sms * 17 / 10;
     int64_t S = (max_tiles + 15) / 16;
-    while (S < max_tiles && S < kMaxCluster && units * (S + 1) <= limit) ++S;
+    while (S < max_tiles && S < kMaxCluster &&
+           units * (S + 1) <= (S + 1 > 4 ? (int64_t)num_sms : (int64_t)num_sms * 17 / 10))
+      ++S;
     const int64_t per = (max_ctx + S - 1) / S;
     p.chunk = (int32_t)((per + kTile - 1) / kTile * kTile);
   }
