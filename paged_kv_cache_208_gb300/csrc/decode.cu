@@ -56,6 +56,7 @@ constexpr unsigned kFull = 0xffffffffu;
 struct Unit {
   int32_t b, s, xg, ntiles;  // ntiles < 0: no more work
   int32_t store;             // store the sequence's new token (its last position) first
+  int32_t skip;              // 1: the ring's next tile is a discarded speculative load
 };
 
 template <int GC>
@@ -174,6 +175,8 @@ __global__ void __maxnreg__(96)
     prefetch_tensormap(&kmap);
     prefetch_tensormap(&vmap);
   }
+  // the first tile's pool row as read ahead of the wait (-1: none), and its KV head
+  int32_t spec_blk = -1, spec_row = -1, spec_h = 0;
   if (!p.queue && threadIdx.x == kConsumerWarps * 32) {
     // Static grid: this CTA's unit is known now. While the previous grid finishes, warm L2
     // with its context length, and with its first tiles through a block id read ahead of the
@@ -190,6 +193,11 @@ __global__ void __maxnreg__(96)
         const int in_block = (int)(begin % p.block_size);
         const int n = min(2 * kStages, min(p.chunk, p.block_size - in_block) / kTile);
         const int h = xg / p.head_groups;
+        if (p.k_new == nullptr) {  // (with the store inside, the last tile waits for it)
+          spec_blk = blk;
+          spec_row = (int32_t)((int64_t)blk * p.block_size + in_block);
+          spec_h = h;
+        }
         for (int t = 0; t < n; ++t) {
           const int32_t row = (int32_t)((int64_t)blk * p.block_size + in_block + t * kTile);
           tma_prefetch_3d(&kmap, 0, row, 2 * h);
@@ -214,10 +222,22 @@ __global__ void __maxnreg__(96)
     bool newkv_pending = false;    // new-token rows on their way into shared memory
     int newkv_slot = 0;
     bool first_unit = true;  // the abort bit is read with the first unit's loads
+    // The first tile's K and V are loaded at once with the block id read ahead of the wait;
+    // once the block table is read again, the tile is kept if the id still holds, else the
+    // consumers discard it (Unit::skip) and the tile is loaded again.
+    bool spec_pending = false;
+    if (spec_row >= 0) {
+      mbar_arrive_expect_tx(&sm.full[0], 2 * kTileBytes);
+      tma_load_3d(sm.k[0], &kmap, &sm.full[0], 0, spec_row, 2 * spec_h, policy);
+      tma_load_3d(sm.v[0], &vmap, &sm.full[0], 0, spec_row, 2 * spec_h, policy);
+      tiles = 1;
+      spec_pending = true;
+    }
     while (ok) {
       // next unit with work (or one that must write zeros); ntiles < 0 ends the walk
-      Unit un{0, 0, 0, -1, 0};
+      Unit un{0, 0, 0, -1, 0, 0};
       int32_t first_blk = -1;  // block id of the unit's first tile
+      int first_it = 0;        // tiles of the unit already loaded
       while (true) {
         int u;
         if (p.queue) {
@@ -260,13 +280,19 @@ __global__ void __maxnreg__(96)
           // the unit that reads position L - 1 stores the new token there first (only one
           // unit per KV head reads it: the launcher takes this path with one head group)
           un = Unit{b, s, xg, (int)((end - begin + kTile - 1) / kTile),
-                    p.k_new != nullptr && end == L ? 1 : 0};
+                    p.k_new != nullptr && end == L ? 1 : 0, 0};
+          if (spec_pending) {
+            if (first_blk == spec_blk) first_it = 1;
+            else un.skip = 1;
+            spec_pending = false;
+          }
           break;
         }
         if (p.cluster || (L == 0 && s == 0 && p.splits == 1)) {
           // nothing to read: zeros (empty context), or in a cluster no result (the unit
           // still leaves its -inf log2-sum-exp for the merge)
-          un = Unit{b, s, xg, 0, 0};
+          un = Unit{b, s, xg, 0, 0, spec_pending ? 1 : 0};
+          spec_pending = false;
           break;
         }
       }
@@ -307,7 +333,7 @@ __global__ void __maxnreg__(96)
       }
       const int32_t *table = p.block_tables + (int64_t)un.b * p.table_width;
       const int tok_begin = un.s * p.chunk;
-      for (int it = 0; it < un.ntiles; ++it, ++tiles) {
+      for (int it = first_it; it < un.ntiles; ++it, ++tiles) {
         const int stage = tiles % kStages;
         if (tiles >= kStages && !wait_parity(&sm.empty[stage], ((tiles / kStages) - 1) & 1, p.err)) {
           ok = false;
@@ -414,7 +440,14 @@ __global__ void __maxnreg__(96)
     for (int m = 0; m < 8; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
 
     bool ok = true;
-    for (int it = 0; it < un.ntiles; ++it, ++tiles) {
+    if (un.skip) {  // a speculative load of the first tile that did not hold: let it land, drop it
+      const int stage = tiles % kStages;
+      ok = __all_sync(kFull, wait_parity(&sm.full[stage], (tiles / kStages) & 1, p.err));
+      __syncwarp();
+      if (ok && lane == 0) mbar_arrive(&sm.empty[stage]);
+      ++tiles;
+    }
+    for (int it = 0; ok && it < un.ntiles; ++it, ++tiles) {
       const int stage = tiles % kStages;
       // warp-uniform: the loop body uses warp-wide MMAs and shuffles
       if (!__all_sync(kFull, wait_parity(&sm.full[stage], (tiles / kStages) & 1, p.err))) {

@@ -6,6 +6,8 @@ span several tiles, splits and blocks with ragged tails, and at the full decode 
 times; plus the invariants: bit-identical results under block permutation and for shared
 vs private prefix blocks, and a one-token context returning V exactly.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -120,6 +122,25 @@ def test_decode_shared_prefix_block_equals_private_copy():
                                                     int(ctx.max()), 128 ** -0.5)))
     assert alloc.ref_count[pre[0]] == 3
     assert np.array_equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("num_splits", [0, 1, 4, 8, 9])
+def test_decode_stale_table_entries_past_context(num_splits):
+    """Table entries past each context hold valid block ids of other sequences (a row left
+    over from an earlier step): nothing past the context may be read. Units whose first
+    tile lies past their context (the kernel may start loading them before it has read the
+    context length) must drop that tile."""
+    lay, val = _host_case([5, 300, 2100, 40], seed=57)  # 9 splits: 288 units, a static grid
+    g = w.rng(58)
+    bt = lay.block_tables.copy()
+    stale = bt < 0
+    bt[stale] = g.integers(0, lay.num_blocks, size=int(stale.sum()))
+    ref = _oracle_step(lay, val)
+    lay_stale = dataclasses.replace(lay, block_tables=bt)
+    out = _gpu_step(lay_stale, dev(val.k_cache), dev(val.v_cache), dev(val.q), dev(val.k_new),
+                    dev(val.v_new), num_splits)
+    assert_attention_close(out, ref, f"stale table entries, splits={num_splits}")
+    assert pkv.get_device_errors() == 0
 
 
 def test_decode_zero_query_is_mean_of_v():
