@@ -71,14 +71,33 @@ struct DecodeSmem {
   Unit unit[kRing];
   alignas(16) uint32_t zero16[4];  // an all-zero ldmatrix row (q rows past GC)
   int32_t stop;  // set by the producer: an earlier wait gave up, this CTA does no work
-  float cl_o[GC][kD];  // cluster merge: this CTA's normalised output and log2-sum-exp
-  float cl_lse[GC];
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t unit_full[kRing];
   uint64_t newkv_full[kRing];
   uint64_t unit_empty[kRing];
+  // cluster merge: in rank 0, the peers' results have landed; in a peer (clusters of more
+  // than kLandSplits), rank 0's `acc` is free for them
+  uint64_t cl_bar;
+  uint64_t cl_ready;
 };
+static_assert(kMaxCluster - 1 <= kConsumerWarps, "the peers' results fit in rank 0's acc");
+
+// Where a cluster's rank 0 receives its peers' results: with up to kLandSplits splits in an
+// area of its own past the fixed layout (two CTAs still fit on an SM), else in its merge
+// buffer `acc`, lent once its own merge has read it. (splits - 1) x GC x kD outputs, then
+// (splits - 1) x GC log2-sum-exps, fp32.
+constexpr int kLandSplits = 4;
+template <int GC>
+__host__ __device__ constexpr size_t land_offset() {
+  return (sizeof(DecodeSmem<GC>) + 15) / 16 * 16;
+}
+template <int GC>
+__host__ __device__ constexpr size_t smem_bytes(int cluster) {
+  return (cluster >= 2 && cluster <= kLandSplits
+              ? land_offset<GC>() + (size_t)(cluster - 1) * GC * (kD + 1) * sizeof(float)
+              : sizeof(DecodeSmem<GC>)) + 1024;  // + 1024: the layout starts 1024-aligned
+}
 
 // Byte offset of 16-byte chunk j (dims 8j..8j+7) of token t inside a swizzled tile. The TMA
 // box is {64 dims, 64 tokens, 2 halves}: half j / 8 of every token in its own 8 KiB plane of
@@ -152,7 +171,6 @@ __global__ void __maxnreg__(96)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  if (threadIdx.x < GC) sm.cl_lse[threadIdx.x] = -INFINITY;  // no result yet
   if (threadIdx.x < 4) sm.zero16[threadIdx.x] = 0u;
   if (threadIdx.x == 0) {
     sm.stop = 0;
@@ -165,9 +183,17 @@ __global__ void __maxnreg__(96)
       mbar_init(&sm.newkv_full[i], 1);
       mbar_init(&sm.unit_empty[i], kConsumerWarps);
     }
+    if (p.cluster) {
+      mbar_init(&sm.cl_bar, p.cluster - 1);  // one arrival per peer
+      mbar_init(&sm.cl_ready, 1);
+    }
     fence_mbar_init();
   }
   __syncthreads();
+  // in a cluster: this CTA's barriers are set up (waited for before the first remote access)
+  if (p.cluster) cluster_arrive_relaxed();
+  // cluster merge: this CTA's normalised output and log2-sum-exp (consumer thread g * kD + d)
+  float cl_o = 0.f, cl_lse = -INFINITY;
   // Launched as a programmatic dependent of the stream's previous kernel: everything above
   // (barrier set-up) may overlap its tail; wait for that grid's completion and memory before
   // touching global memory.
@@ -556,8 +582,8 @@ __global__ void __maxnreg__(96)
       }
       const int64_t row = (int64_t)un.b * p.num_q_heads + hq0 + g;
       if (p.cluster) {  // merged by the cluster's rank 0 at the end
-        sm.cl_o[g][d] = o;
-        if (d == 0) sm.cl_lse[g] = lse;  // -inf when the unit had no keys
+        cl_o = o;
+        cl_lse = lse;  // -inf when the unit had no keys
       } else if (p.splits == 1) {
         p.out[row * kD + d] = bf16_bits_rn(o);
       } else {
@@ -571,46 +597,58 @@ __global__ void __maxnreg__(96)
   }
   if (!p.cluster) return;
   // ---------------------------------------------------------------- cluster merge
-  // Every CTA of the cluster (one per split of this sequence and head group) has its result
-  // in shared memory; rank 0 reads them through distributed shared memory and writes the
-  // output, the others stay until it has read theirs.
-  cluster_sync();
-  if (cluster_ctarank() == 0 && threadIdx.x < GC * kD) {
-    const int g = threadIdx.x / kD, d = threadIdx.x % kD;
-    // all loads first (one round trip), then release the peers
-    const uint32_t lse_a = smem_addr(&sm.cl_lse[g]), o_a = smem_addr(&sm.cl_o[g][d]);
-    float l[kMaxCluster], o[kMaxCluster];
-#pragma unroll
-    for (int r = 0; r < kMaxCluster; ++r) {
-      l[r] = -INFINITY;
-      o[r] = 0.f;
-      if (r < p.splits) {
-        l[r] = ld_cluster_f32(cluster_addr(lse_a, r));
-        o[r] = ld_cluster_f32(cluster_addr(o_a, r));
-      }
-    }
-    cluster_arrive();  // the peers' shared memory is no longer needed
-    float M = -INFINITY;
-#pragma unroll
-    for (int r = 0; r < kMaxCluster; ++r) M = fmaxf(M, l[r]);
-    float acc = 0.f, wsum = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int r = 0; r < kMaxCluster; ++r) {
-        const float wgt = fast_exp2(l[r] - M);  // 0 for a split with no keys (and r >= splits)
-        wsum += wgt;
-        acc = fmaf(wgt, o[r], acc);
-      }
-    }
-    const int unit0 = blockIdx.x;  // rank 0 holds split 0
-    const int b = (unit0 / p.splits) / p.xgroups, xg = (unit0 / p.splits) % p.xgroups;
-    const int h = xg / p.head_groups;
-    const int64_t row = (int64_t)b * p.num_q_heads + h * p.group + (xg % p.head_groups) * GC + g;
-    if (!sm.stop) p.out[row * kD + d] = bf16_bits_rn(wsum > 0.f ? acc / wsum : 0.f);
-  } else {
-    cluster_arrive();
+  // The CTAs of the cluster are the splits of one sequence and head group. Each peer sends
+  // its result into rank 0's landing area (for more than kLandSplits splits, rank 0's merge
+  // buffer, which rank 0 lends once its own merge has read it) with asynchronous stores
+  // counted on rank 0's barrier and leaves; rank 0 waits for the bytes, merges and writes the
+  // output. (Rank 0 never reads a peer's memory, so the peers need not wait for it to
+  // finish.) The waits below ignore the abort bit: every CTA reaches this point (its other
+  // waits are bounded), rank 0 always lends the buffer and every peer always sends, so no
+  // store lands in a CTA that has left.
+  cluster_wait();  // every CTA's barriers are set up
+  if (threadIdx.x >= GC * kD) return;
+  const uint32_t rank = cluster_ctarank();
+  const bool lend = p.cluster > kLandSplits;
+  float *land_o = lend ? &sm.acc[0][0][0]  // peer r + 1's outputs at [r][g][d], then its lses
+                       : reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(&sm) +
+                                                   land_offset<GC>());
+  float *land_lse = land_o + (size_t)(p.cluster - 1) * GC * kD;
+  const int g = threadIdx.x / kD, d = threadIdx.x % kD;
+  if (rank != 0) {
+    if (lend && !wait_own(&sm.cl_ready, 0, p.err)) return;
+    const uint32_t bar = cluster_addr(smem_addr(&sm.cl_bar), 0);
+    if (threadIdx.x == 0) mbar_arrive_expect_tx_remote(bar, GC * (kD + 1) * sizeof(float));
+    const int r = (int)rank - 1;
+    st_async_f32(cluster_addr(smem_addr(land_o + ((size_t)r * GC + g) * kD + d), 0), cl_o, bar);
+    if (d == 0) st_async_f32(cluster_addr(smem_addr(land_lse + r * GC + g), 0), cl_lse, bar);
+    return;
   }
-  cluster_wait();
+  if (lend) {
+    // every merging thread has read `acc` (its values are in registers): lend it to the peers
+    named_barrier_sync(2, GC * kD);
+    if (threadIdx.x == 0)
+      for (int r = 1; r < p.cluster; ++r)
+        mbar_arrive_remote(cluster_addr(smem_addr(&sm.cl_ready), r));
+  }
+  if (!wait_own(&sm.cl_bar, 0, p.err)) return;
+  float M = cl_lse;
+  for (int r = 0; r < p.cluster - 1; ++r) M = fmaxf(M, land_lse[r * GC + g]);
+  float acc = 0.f, wsum = 0.f;
+  if (M != -INFINITY) {
+    const float w0 = fast_exp2(cl_lse - M);  // 0 for a split with no keys
+    wsum = w0;
+    acc = w0 * cl_o;
+    for (int r = 0; r < p.cluster - 1; ++r) {
+      const float wgt = fast_exp2(land_lse[r * GC + g] - M);
+      wsum += wgt;
+      acc = fmaf(wgt, land_o[((size_t)r * GC + g) * kD + d], acc);
+    }
+  }
+  const int unit0 = blockIdx.x;  // rank 0 holds split 0
+  const int b = (unit0 / p.splits) / p.xgroups, xg = (unit0 / p.splits) % p.xgroups;
+  const int h = xg / p.head_groups;
+  const int64_t row = (int64_t)b * p.num_q_heads + h * p.group + (xg % p.head_groups) * GC + g;
+  if (!sm.stop) p.out[row * kD + d] = bf16_bits_rn(wsum > 0.f ? acc / wsum : 0.f);
 }
 
 // One warp per (sequence, query head): out = sum_s 2^(lse_s - lse) o_s over the sequence's
@@ -661,13 +699,14 @@ __global__ void __launch_bounds__(128)
 template <int GC>
 cudaError_t launch_split(const CUtensorMap &km, const CUtensorMap &vm, const DecodeParams &prm,
                          int num_sms, cudaStream_t stream) {
-  const size_t smem = sizeof(DecodeSmem<GC>) + 1024;
+  const size_t smem = smem_bytes<GC>(prm.cluster);
   static bool configured[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !configured[dev]) {
     cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<GC>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem_bytes<GC>(kLandSplits));
     if (e != cudaSuccess) return e;
     // all of the unified L1/shared storage as shared memory, so two CTAs fit on an SM
     e = cudaFuncSetAttribute(decode_split_kernel<GC>,

@@ -148,10 +148,33 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster_addr) {
                : "memory");
 }
 
-__device__ __forceinline__ float ld_cluster_f32(uint32_t cluster_addr_) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr_) : "memory");
-  return v;
+// The arrive half of a cluster barrier with no memory ordering (for "every CTA has set up
+// its barriers", before any remote access).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+// Asynchronous 4-byte store into a CTA of the cluster whose bytes count on an mbarrier of that
+// CTA (complete_tx): the barrier's phase completes only once the data has landed, and a
+// thread that sees the phase complete sees the data.
+__device__ __forceinline__ void st_async_f32(uint32_t cluster_addr_, float v,
+                                             uint32_t bar_cluster_addr) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
+          cluster_addr_),
+      "r"(__float_as_uint(v)), "r"(bar_cluster_addr)
+      : "memory");
+}
+
+// Arrive on an mbarrier of a CTA of the cluster and raise its expected transaction bytes,
+// with no ordering of this thread's other memory operations (the bytes come by complete_tx).
+__device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t bar_cluster_addr,
+                                                             uint32_t bytes) {
+  asm volatile(
+      "mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
+          bar_cluster_addr),
+      "r"(bytes)
+      : "memory");
 }
 
 __device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr_, uint4 v) {
