@@ -577,8 +577,10 @@ __global__ void __maxnreg__(96)
           lsum = fmaf(sm.l[w][g], f, lsum);
           osum = fmaf(sm.acc[w][g][d], f, osum);
         }
-        o = osum / lsum;
-        lse = M + log2f(lsum);
+        // lsum >= 1 (the warp holding the maximum contributes 2^0): the approximate division
+        // and log2 err far below one bf16 rounding of the result
+        o = __fdividef(osum, lsum);
+        lse = M + __log2f(lsum);
       }
       const int64_t row = (int64_t)un.b * p.num_q_heads + hq0 + g;
       if (p.cluster) {  // merged by the cluster's rank 0 at the end
