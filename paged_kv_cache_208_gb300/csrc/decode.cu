@@ -12,24 +12,25 @@
 // Persistent kernel: two CTAs per SM take units from a global queue (one atomic counter in
 // the workspace; units ordered split-major with the KV heads of a sequence adjacent, so the
 // CTAs reading one sequence's rows run together). When there are no more units than CTAs,
-// CTA i takes unit i and the counter is not used. Per CTA, 8 consumer warps + 1 producer
-// warp:
+// CTA i takes unit i and the counter is not used (a static grid). Per CTA, 8 consumer warps
+// + 1 producer warp:
 //   producer  -- takes a unit, hands it to the consumers through a 4-slot ring (the unit's
 //                q rows arrive by a 1-D bulk copy into the ring slot), then streams the
 //                unit's tiles: per 64-token tile it looks up block_tables[b][pos / bs] and
-//                issues two TMA tensor loads (K and V, 64 tokens x 256 bytes of head h,
-//                128-byte swizzled) into a 3-stage ring, without stopping between units;
-//   consumers -- warp w owns tokens [8w, 8w + 8) of every tile with its own online softmax:
-//                  QK:  4 lanes per token, 32 dims per lane, mixed-precision bf16 FMAs on
-//                       packed q (no conversions), reduced with 2 shuffles;
-//                  PV:  16 lanes per token (8 dims each), two tokens per instruction,
-//                       packed fp32x2 FMAs;
-//                at the end of a unit the 8 warp states are merged through shared memory.
+//                issues two TMA tensor loads (K and V, 64 tokens x 256 bytes of head h, as two
+//                128-byte-swizzled planes of 64 dims) into a 3-stage ring, without stopping
+//                between units. On a static grid it reads its unit's first block id before
+//                the grid dependency wait and loads that tile right after it (dropped again
+//                if the block table, read again, names another block);
+//   consumers -- warp w owns tokens [8w, 8w + 8) of every tile; both products are warp MMAs
+//                with the unit's query heads as the M rows (see the consumer section), with
+//                the warp's own online softmax; at the end of a unit the 8 warp states are
+//                merged through shared memory.
 // With one split a unit writes bf16 output. With 2..8 splits and a static grid (one CTA per
 // unit, units ordered split-minor), the splits of one (sequence, head group) form a
-// thread-block cluster: each CTA leaves its normalised partial output and log2-sum-exp in its
-// own shared memory and the cluster's rank 0 merges them through distributed shared memory.
-// Otherwise a unit writes its partial to global memory and decode_combine_kernel merges.
+// thread-block cluster: each peer sends its normalised partial output and log2-sum-exp into
+// rank 0's shared memory with asynchronous stores and rank 0 merges them. Otherwise a unit
+// writes its partial to global memory and decode_combine_kernel merges.
 //
 // Algorithmic HBM bytes per (sequence, KV head, token): 256 (K) + 256 (V).
 #include <math.h>
