@@ -587,7 +587,9 @@ __global__ void __maxnreg__(96)
       if (p.cluster) {  // merged by the cluster's rank 0 at the end
         cl_o = o;
         cl_lse = lse;  // -inf when the unit had no keys
-      } else if (p.splits == 1) {
+      } else if (p.splits == 1 || (un.s == 0 && tok_end == L)) {
+        // the unit holds the whole context: the output itself (the merge kernel skips rows
+        // whose context fits one split)
         p.out[row * kD + d] = bf16_bits_rn(o);
       } else {
         p.part_o[(row * p.splits + un.s) * kD + d] = o;
@@ -655,7 +657,8 @@ __global__ void __maxnreg__(96)
 }
 
 // One warp per (sequence, query head): out = sum_s 2^(lse_s - lse) o_s over the sequence's
-// splits, lse = log2 sum_s 2^lse_s. A sequence with no token gets zeros.
+// splits, lse = log2 sum_s 2^lse_s. A sequence with no token gets zeros; one whose context
+// fits one split was written by the split kernel.
 __global__ void __launch_bounds__(128)
     decode_combine_kernel(const float *__restrict__ part_o, const float *__restrict__ part_lse,
                           const int32_t *__restrict__ context_lens, int32_t batch,
@@ -675,6 +678,7 @@ __global__ void __launch_bounds__(128)
   int64_t L = context_lens[b];
   L = L < 0 ? 0 : (L > cap ? cap : L);
   const int ns = (int)((L + chunk - 1) / chunk);
+  if (ns == 1) return;  // one split: the split kernel wrote this row itself
   const float *lse = part_lse + row * splits;
   float M = -INFINITY;
   for (int s = lane; s < ns; s += 32) M = fmaxf(M, lse[s]);
