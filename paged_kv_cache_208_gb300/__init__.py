@@ -92,8 +92,15 @@ def _check(fn: str, status: int) -> None:
         raise PkvError(fn, status)
 
 
+# The current stream's cudaStream_t for a device index, without building a Stream object
+# (several microseconds a call); the public query when this torch lacks it.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream) -> int:
     if stream is None:
+        if _raw_stream is not None:
+            return int(_raw_stream(torch.cuda.current_device()))
         stream = torch.cuda.current_stream()
     return int(stream.cuda_stream if hasattr(stream, "cuda_stream") else stream)
 
