@@ -235,3 +235,17 @@ def test_decode_batch_sweep(batch):
     lay = w.sweep_decode_layout(batch, num_blocks=batch * 4 + 16)
     rows = np.arange(batch) if batch <= 64 else w.rng(batch).choice(batch, 64, replace=False)
     _full_size(lay, 3000 + batch, check_rows=np.sort(rows))
+
+
+def test_decode_runs_on_the_callers_current_stream():
+    """With no stream given, the binding launches on torch's current stream: a side stream's
+    handle is what it passes, and a call made under that stream sees the inputs written on it."""
+    lay, val = _host_case([300, 1200], seed=59)
+    ref = _oracle_step(lay, val)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        assert pkv._stream(None) == s.cuda_stream
+        kc, vc = dev(val.k_cache), dev(val.v_cache)
+        out = _gpu_step(lay, kc, vc, dev(val.q), dev(val.k_new), dev(val.v_new))
+    s.synchronize()
+    assert_attention_close(out, ref, "side stream")
