@@ -82,6 +82,21 @@ def test_abort_bit_stops_every_kernel_and_clearing_it_recovers():
         pkv.varlen_prefill_attn(dev(q_p), dev(k_p), dev(v_p), dev(cu), dev(cu), 300, 300,
                                 128 ** -0.5, out=out_p)
         assert _untouched(out_p), "prefill wrote while aborted"
+        # QK-norm + RoPE + store: neither q nor the pools are written
+        T = int(cu[-1])
+        qkv = dev(w.host_bf16_normal(g, (T, (16 + 2 * 8) * 128)))
+        ones = torch.ones(128, dtype=torch.bfloat16, device="cuda")
+        table = torch.from_numpy(w.random_cos_sin_table(g, 512, 128)).cuda()
+        pos = torch.arange(T, dtype=torch.int64, device="cuda") % 512
+        slots = torch.arange(T, dtype=torch.int64, device="cuda")
+        kc_r = _filled_like(torch.empty((-(-T // 256), 256, 8, 128), dtype=torch.bfloat16,
+                                        device="cuda"))
+        vc_r = _filled_like(kc_r)
+        q_r = _filled_like(torch.empty((T, 16, 128), dtype=torch.bfloat16, device="cuda"))
+        pkv.qk_norm_rope_store(qkv, pos, ones, ones, 1e-6, table, slots, kc_r, vc_r, 16, 8,
+                               q_out=q_r)
+        assert _untouched(q_r) and _untouched(kc_r) and _untouched(vc_r), \
+            "qk_norm_rope_store wrote while aborted"
         assert pkv.get_device_errors(reset=False) == pkv.DEVERR_TIMEOUT
     finally:
         pkv.get_device_errors(reset=True)
