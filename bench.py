@@ -751,8 +751,9 @@ def run_profile(args):
     """One kernel alone on its workload, for ncu: `decode` (the Qwen3 batch, one layer, a pool
     of just the referenced blocks: 1.2 GB, larger than L2), `decode_small` (--profile-batch
     sequences of 1024 tokens, graph-replayed), `decode_long` (8 x 32768), `prefill` (the varlen workload,
-    packed), `prefix` (the prefix-cached workload, keys through block_table) or `store` (the
-    varlen workload's kv_store). Runs --warmup + --steps launches."""
+    packed), `prefill_long` (16 prompts of 8192 tokens, packed), `prefix` (the prefix-cached
+    workload, keys through block_table) or `store` (the varlen workload's kv_store). Runs
+    --warmup + --steps launches."""
     torch.cuda.set_device(0)
     pkv = load_pkv()
     if args.profile == "decode":
@@ -808,7 +809,8 @@ def run_profile(args):
         run = lambda: pkv.varlen_prefill_attn(q, kc, vc, cq, ck, mq, mk, D ** -0.5, out=out,
                                               block_table=bt)
     else:
-        lens = w.varlen_prefill_lengths()
+        lens = (np.full(16, 8192, np.int32) if args.profile == "prefill_long"
+                else w.varlen_prefill_lengths())
         cu = torch.from_numpy(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)).cuda()
         T = int(lens.sum())
         q = w.device_bf16_normal((T, HQ, D), 401)
@@ -842,7 +844,7 @@ def main():
     ap.add_argument("--profile-batch", type=int, default=8,
                     help="sequences for --profile decode_small")
     ap.add_argument("--profile", choices=["decode", "decode_small", "decode_long", "prefill",
-                                          "prefix", "store", "rope"],
+                                          "prefill_long", "prefix", "store", "rope"],
                     help="run one kernel alone (for ncu); prints no benchmark line")
     args = ap.parse_args()
     if args.warmup < 3:
