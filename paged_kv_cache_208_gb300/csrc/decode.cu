@@ -761,15 +761,19 @@ DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
     p.chunk = (int32_t)((per + kTile - 1) / kTile * kTile);
   } else {
     // At most 16 tiles per unit (a CTA streams its unit through a 3-tile ring, so long
-    // units cap the bandwidth of a skewed batch; the work queue balances short ones). Below
-    // that, more splits give more CTAs for a small batch, but every CTA past one per SM
-    // shares an SM, and a unit's fixed costs (its first tile's latency, the merges) do not
-    // shrink. Measured on batches 1..64 at 1024 tokens, the best split count is the largest
-    // that keeps its splits within one cluster and the grid within about 1.7 CTAs per SM,
-    // or within one CTA per SM for clusters of more than 4 (larger clusters do not all fit
-    // at once when SMs hold two CTAs).
+    // units cap the bandwidth of a skewed batch; the work queue balances short ones), or 32
+    // once there are at least 8 units per SM: then the queue hides the long units' tail, and
+    // one split fewer saves the partial results and the merge (Qwen3 batch, 256 contexts up
+    // to 2048 tokens: 1 split 178.5 us per call against 179.9 us with 2). Below that, more
+    // splits give more CTAs for a small batch, but every CTA past one per SM shares an SM,
+    // and a unit's fixed costs (its first tile's latency, the merges) do not shrink.
+    // Measured on batches 1..64 at 1024 tokens, the best split count is the largest that
+    // keeps its splits within one cluster and the grid within about 1.7 CTAs per SM, or
+    // within one CTA per SM for clusters of more than 4 (larger clusters do not all fit at
+    // once when SMs hold two CTAs).
     const int64_t units = (int64_t)batch * num_kv_heads * p.head_groups;
-    int64_t S = (max_tiles + 15) / 16;
+    const int64_t max_unit_tiles = units >= 8LL * num_sms ? 32 : 16;
+    int64_t S = (max_tiles + max_unit_tiles - 1) / max_unit_tiles;
     while (S < max_tiles && S < kMaxCluster &&
            units * (S + 1) <= (S + 1 > 4 ? (int64_t)num_sms : (int64_t)num_sms * 17 / 10))
       ++S;
