@@ -668,7 +668,7 @@ def run_ours(args):
         "kv_tokens_per_s": step.kv_tokens * world / per_step,
         "decode_frac_of_hbm_peak": achieved / hbm_peak,
         "roofline": {"bound": "hbm",
-                     "kernel": "paged_decode_step (split kernel with the store, + combine)",
+                     "kernel": "paged_decode_step (split kernel with the store; + the merge kernel when contexts are split)",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "peak_source": peak_src,
                      "traffic": traffic,
