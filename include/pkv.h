@@ -63,6 +63,10 @@ typedef int32_t pkv_status;
                                          while it is set, every attention kernel of the library
                                          returns at once without computing, until
                                          pkv_get_device_errors(&e, 1) clears it. */
+#define PKV_DEVERR_WORKSPACE 64u      /* decode: the work counter at the start of the workspace
+                                         held a value that a zeroed counter cannot give: it
+                                         was not zero when the call started, and outputs may
+                                         be missing. Zero it again (cudaMemsetAsync). */
 
 /* Human-readable name of a status code. Never NULL; the string is static. */
 const char *pkv_status_string(pkv_status status);
@@ -119,8 +123,9 @@ pkv_status pkv_kv_store(const void *k, int64_t k_tok_stride, const void *v, int6
  * `num_splits` must be the value later passed to the call (0 = automatic choice, made from
  * the sizes and the current device's SM count). The workspace holds each split's partial
  * output [batch, num_q_heads, splits, head_dim] fp32 and its log-sum-exp [batch,
- * num_q_heads, splits] fp32 (when there is more than one split), then the persistent
- * kernel's work counter, which the call resets on its stream. Returns 0 for invalid sizes.
+ * num_q_heads, splits] fp32 (when there is more than one split), after a 16-byte header
+ * that holds the persistent kernel's work counter (see the workspace argument below: it must
+ * be zero before the first call). Returns 0 for invalid sizes.
  */
 size_t pkv_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                   int32_t head_dim, int32_t max_context_len,
@@ -151,8 +156,14 @@ size_t pkv_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t nu
  *                physical placement of the blocks; they differ by rounding across values of
  *                num_splits.
  * workspace:     pkv_decode_workspace_bytes(...) bytes, 16-byte aligned, private to this
- *                call while it runs (calls that may overlap need separate workspaces).
- *                Contents on entry are ignored.
+ *                call while it runs (calls that may overlap need separate workspaces). Its
+ *                first 4 bytes are the persistent kernel's work counter: it must be zero
+ *                before the workspace's first call (e.g. cudaMemsetAsync of the first 16
+ *                bytes once after allocating it), and every call leaves it at zero again,
+ *                so calls on the same stream need nothing in between, also in a captured
+ *                CUDA graph. With a counter that was not zero the results are undefined
+ *                (never a fault); values that a zeroed counter cannot give set
+ *                PKV_DEVERR_WORKSPACE. The rest of the workspace is scratch.
  * out:           [batch, num_q_heads, head_dim] bf16.
  * Implemented: head_dim == 128, block_size a multiple of 256 (the pages: block size must be
  * a multiple of 256), any num_q_heads / num_kv_heads, q, pools and out 16-byte aligned.
@@ -272,15 +283,17 @@ pkv_status pkv_varlen_prefill_attn(const void *q, int64_t q_tok_stride, int64_t 
  * the array (pkv_decode_workspace_bytes(...) > PKV_DECODE_NOALLOC_SCRATCH_BYTES) is rejected
  * with PKV_ERR_WORKSPACE before anything is enqueued; choosing fewer splits (num_splits > 0)
  * or the workspace entry point avoids that. The automatic plan of the Qwen3-shaped batch (256
- * sequences x 16 query heads, contexts up to 2048) needs about 17 MB.
+ * sequences x 16 query heads, contexts up to 2048) takes one split and needs only the 16-byte
+ * header; two splits need about 4.2 MB.
  *
  * The first call on each device looks up the array's device address (cudaGetSymbolAddress,
  * with that device current) and caches it; make that first call before any stream capture.
  * A lookup that fails returns PKV_ERR_CUDA, is not cached (the next call tries again) and
  * leaves no pending CUDA error behind.
- * All calls on a device share the array and it keeps the last call's contents (nothing needs
- * to start at zero). Calls whose kernels may run at the same time on the GPU (different
- * streams without ordering) race on the array: order them on one stream.
+ * All calls on a device share the array. Its work counter starts at zero, and every call
+ * leaves it at zero again (as with a workspace). Calls whose kernels may run at the same time
+ * on the GPU (different streams without ordering) race on the array: order them on one
+ * stream.
  */
 #define PKV_DECODE_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 

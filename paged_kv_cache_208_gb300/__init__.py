@@ -22,6 +22,7 @@ LIB_PATH = os.path.join(_HERE, "libpkv.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_NO_BLOCKS = range(6)
 DEVERR_SLOT_RANGE, DEVERR_BLOCK_RANGE, DEVERR_CONTEXT_RANGE = 1, 2, 4
 DEVERR_SEQLEN_RANGE, DEVERR_TIMEOUT, DEVERR_POSITION_RANGE = 8, 16, 32
+DEVERR_WORKSPACE = 64
 
 # symbol -> (restype, argtypes); mirrors include/pkv.h
 _P, _I32, _I64, _F, _SZ = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
@@ -160,9 +161,11 @@ def decode_workspace_bytes(batch: int, num_q_heads: int, num_kv_heads: int, head
 
 def decode_workspace(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
                      max_context_len: int, num_splits: int = 0, device=None) -> torch.Tensor:
+    """A decode workspace, zeroed: its first 16 bytes are work counters that must be zero
+    before the first call (every call leaves them zero again)."""
     n = decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, max_context_len,
                                num_splits)
-    return torch.empty(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device or "cuda")
 
 
 def paged_decode_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,

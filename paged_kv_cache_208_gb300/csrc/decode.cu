@@ -9,10 +9,12 @@
 // [s * chunk, min((s + 1) * chunk, ctx_b)). chunk is a multiple of the 64-token tile and the
 // block size a multiple of 256, so a tile never straddles a block.
 //
-// Persistent kernel: two CTAs per SM take units from a global queue (one atomic counter in
-// the workspace; units ordered split-major with the KV heads of a sequence adjacent, so the
-// CTAs reading one sequence's rows run together). When there are no more units than CTAs,
-// CTA i takes unit i and the counter is not used (a static grid). Per CTA, 8 consumer warps
+// Persistent kernel: two CTAs per SM take units from a global queue (an atomic counter at the
+// start of the workspace; units ordered split-major with the KV heads of a sequence adjacent,
+// so the CTAs reading one sequence's rows run together). Every CTA draws until it draws past
+// the last unit, once; the CTA whose draw is the last of those sets the counter back to
+// zero, so no call has to clear it first. When there are no more units than CTAs, CTA i takes
+// unit i and the counter is not used (a static grid). Per CTA, 8 consumer warps
 // + 1 producer warp:
 //   producer  -- takes a unit, hands it to the consumers through a 4-slot ring (the unit's
 //                q rows arrive by a 1-D bulk copy into the ring slot), then streams the
@@ -47,6 +49,7 @@ constexpr int kD = 128;
 constexpr int kTile = 64;
 constexpr int kConsumerWarps = 8;
 constexpr int kStages = 3;
+constexpr unsigned int kErrWorkspace = 64u;  // PKV_DEVERR_WORKSPACE
 constexpr int kRing = 4;
 constexpr int kMaxCluster = 8;  // largest portable thread-block cluster
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
@@ -116,7 +119,8 @@ struct DecodeParams {
   float *part_o;
   float *part_lse;
   uint16_t *out;
-  int32_t *queue;  // next unit to hand out; nullptr: CTA i takes unit i only
+  int32_t *queue;  // next unit to hand out (the workspace's first word); nullptr: CTA i takes
+                   // unit i only
   // > 0: the splits of one (sequence, head group) form a cluster of this many CTAs (CTA i
   // takes unit i, ordered split-minor); rank 0 merges them through distributed shared memory
   int32_t cluster;
@@ -249,6 +253,24 @@ __global__ void __maxnreg__(96)
     bool newkv_pending = false;    // new-token rows on their way into shared memory
     int newkv_slot = 0;
     bool first_unit = true;  // the abort bit is read with the first unit's loads
+    // The work counter (queued grid). Every CTA draws until it draws past the last unit, once:
+    // those draws return units .. units + grid - 1, so the CTA with the highest one is the
+    // last to touch the counter, and it sets the counter back to zero for the next call. From
+    // a zeroed counter a CTA's first draw is below units + grid: anything else (or a draw
+    // below zero) means the workspace's counter was not zero on entry.
+    bool first_draw = true, past_end = false;
+    auto draw = [&]() -> int {
+      const int u = atomicAdd(p.queue, 1);
+      if (first_draw) {
+        first_draw = false;
+        if (u < 0 || u >= p.units + (int)gridDim.x) record_error(p.err, kErrWorkspace);
+      }
+      if (u < 0 || u >= p.units) {
+        past_end = true;
+        if (u == p.units + (int)gridDim.x - 1) atomicExch(p.queue, 0);
+      }
+      return u;
+    };
     // The first tile's K and V are loaded at once with the block id read ahead of the wait;
     // once the block table is read again, the tile is kept if the id still holds, else the
     // consumers discard it (Unit::skip) and the tile is loaded again.
@@ -268,12 +290,12 @@ __global__ void __maxnreg__(96)
       while (true) {
         int u;
         if (p.queue) {
-          u = atomicAdd(p.queue, 1);
+          u = draw();
         } else {
           u = static_next;
           static_next = p.units;
         }
-        if (u >= p.units) break;
+        if (u < 0 || u >= p.units) break;
         int s, b, xg;
         unit_coords(p, u, s, b, xg);
         // the first tile's block id does not depend on the context length: both loads are in
@@ -397,6 +419,10 @@ __global__ void __maxnreg__(96)
 
       }
     }
+    // a CTA that stopped early (an abort, a wait that gave up) still draws past the last unit
+    // once, so that the counter goes back to zero
+    if (p.queue)
+      while (!past_end) draw();
     // keep the CTA alive until every copy it issued has landed (also after an abort: these
     // waits ignore the abort bit; `tiles` and `pushed` count only issued copies)
     bool drained = true;
@@ -783,7 +809,7 @@ DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
   p.splits = (int32_t)((max_ctx + p.chunk - 1) / p.chunk);
   const size_t partials =
       p.splits > 1 ? (size_t)batch * num_q_heads * p.splits * (kD + 1) * sizeof(float) : 0;
-  p.workspace_bytes = (partials + 15) / 16 * 16 + kDecodeQueueBytes;  // + the work queue
+  p.workspace_bytes = kDecodeQueueBytes + (partials + 15) / 16 * 16;  // the counters first
   return p;
 }
 
@@ -805,16 +831,16 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &p, cudaSt
     return cudaErrorInvalidValue;
 
   uint8_t *ws = static_cast<uint8_t *>(a.workspace);
-  const size_t partials = p.workspace_bytes - kDecodeQueueBytes;
+  float *const part_base = reinterpret_cast<float *>(ws + kDecodeQueueBytes);  // after the counter
   DecodeParams prm{};
   prm.q = static_cast<const uint16_t *>(a.q);
   prm.block_tables = a.block_tables;
   prm.context_lens = a.context_lens;
-  prm.part_o = p.splits > 1 ? reinterpret_cast<float *>(ws) : nullptr;
+  prm.part_o = p.splits > 1 ? part_base : nullptr;
   prm.part_lse = p.splits > 1 ? prm.part_o + (size_t)a.batch * a.num_q_heads * p.splits * kD
                               : nullptr;
   prm.out = static_cast<uint16_t *>(a.out);
-  prm.queue = reinterpret_cast<int32_t *>(ws + partials);
+  prm.queue = reinterpret_cast<int32_t *>(ws);
   prm.err = a.err;
   prm.num_blocks = a.num_blocks;
   prm.cap = std::min((int64_t)a.table_width * a.block_size, (int64_t)p.splits * p.chunk);
@@ -851,14 +877,15 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &p, cudaSt
     }
   }
 
-  // With no more units than CTAs each CTA takes unit blockIdx.x and the counter (and the
-  // memset that resets it) is not needed. Then, with 2 to kMaxCluster splits, the splits of
-  // one (sequence, head group) run as one thread-block cluster and merge in distributed
-  // shared memory: no partials in global memory and no merge kernel.
+  // With no more units than CTAs each CTA takes unit blockIdx.x and the counters are not
+  // used. Then, with 2 to kMaxCluster splits, the splits of one (sequence, head group) run as
+  // one thread-block cluster and merge in distributed shared memory: no partials in global
+  // memory and no merge kernel. With the queue the kernel leaves the counters at zero
+  // itself, so the call enqueues nothing before it (the kernel follows the previous one as a
+  // programmatic dependent).
   const bool queued = (int64_t)a.num_sms * 2 < units;
   cudaError_t e = cudaSuccess;
-  if (queued) e = cudaMemsetAsync(prm.queue, 0, sizeof(int32_t), stream);
-  else prm.queue = nullptr;
+  if (!queued) prm.queue = nullptr;
   if (e != cudaSuccess) return e;
   prm.cluster = !queued && p.splits >= 2 && p.splits <= kMaxCluster ? p.splits : 0;
   e = p.heads_per_cta == 2 ? launch_split<2>(km, vm, prm, a.num_sms, stream)

@@ -54,7 +54,7 @@ struct DecodeArgs {
   const int64_t *slot_mapping = nullptr;
   int64_t num_slots = 0;
 };
-constexpr size_t kDecodeQueueBytes = 16;  // the persistent kernel's work counter
+constexpr size_t kDecodeQueueBytes = 16;  // the workspace's header: the work counters
 cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &plan,
                                 cudaStream_t stream);
 

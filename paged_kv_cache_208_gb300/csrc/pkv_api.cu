@@ -114,7 +114,7 @@ const char *pkv_status_string(pkv_status status) {
   }
 }
 
-int32_t pkv_abi_version(void) { return 1; }
+int32_t pkv_abi_version(void) { return 2; }
 
 pkv_status pkv_raise_device_errors(uint32_t bits) {
   if (!device_info()) return PKV_ERR_CUDA;

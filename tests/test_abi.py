@@ -31,7 +31,7 @@ def test_status_strings():
     for code in range(5):
         assert L.pkv_status_string(code)
     assert L.pkv_status_string(99) == b"unknown status"
-    assert L.pkv_abi_version() == 1
+    assert L.pkv_abi_version() == 2
 
 
 def test_store_argument_checks():

@@ -196,6 +196,39 @@ def test_decode_workspace_too_small_is_rejected():
     assert e.value.status == pkv.ERR_WORKSPACE
 
 
+def test_decode_workspace_counter_left_zero_and_dirty_counter_flagged():
+    """With more units than two per SM the CTAs take units from the work counter at the
+    start of the workspace, and the CTA that draws last sets it back to zero: calls in a row
+    on one workspace need nothing in between. A counter that was not zeroed gives undefined
+    results but no fault (a draw below zero ends a CTA's walk); values that a zeroed counter
+    cannot give (far past the units, or below zero) set DEVERR_WORKSPACE, and once the
+    counter is zeroed again the call is correct."""
+    ctx = [700 + 13 * i for i in range(48)]  # 48 sequences x 8 KV heads: 384 units
+    lay, val = _host_case(ctx, seed=74)
+    oracle.kv_store(val.k_new, val.v_new, lay.slot_mapping, val.k_cache, val.v_cache)
+    q, kc, vc = dev(val.q), dev(val.k_cache), dev(val.v_cache)
+    bt, cl = dev(lay.block_tables), dev(lay.context_lens)
+    ref = oracle.paged_decode(val.q, val.k_cache, val.v_cache, lay.block_tables,
+                              lay.context_lens, lay.scale)
+    ws = pkv.decode_workspace(lay.batch, 16, 8, 128, lay.max_context_len, 0)
+    call = lambda: pkv.paged_decode_attn(q, kc, vc, bt, cl, lay.max_context_len, lay.scale,
+                                         workspace=ws)
+    pkv.get_device_errors(reset=True)
+    for i in range(3):
+        assert_attention_close(call(), ref, f"call {i} on the same workspace")
+        assert int(ws[:16].count_nonzero()) == 0
+    assert pkv.get_device_errors() == 0
+    for garbage in (1 << 20, -(1 << 30)):
+        ws[:16].view(torch.int32)[0] = garbage
+        call()
+        torch.cuda.synchronize()
+        assert pkv.get_device_errors(reset=True) & pkv.DEVERR_WORKSPACE, garbage
+        ws.zero_()
+        assert_attention_close(call(), ref, f"zeroed again after a counter of {garbage}")
+        assert int(ws[:16].count_nonzero()) == 0
+        assert pkv.get_device_errors() == 0
+
+
 # ------------------------------------------------------------------ full-size workloads
 def _full_size(lay, seed, check_rows=None):
     """Device pools drawn on the GPU; the new token stored, decode run with the automatic
