@@ -54,6 +54,9 @@ constexpr int kRing = 4;
 constexpr int kMaxCluster = 8;  // largest portable thread-block cluster
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kTileBytes = kTile * kD * 2;  // one head's K (or V) for 64 tokens: 16 KiB
+constexpr int kPlaneBytes = kTileBytes / 2;  // one 64-dim half of it (a plane of 64 rows)
+constexpr int kChunkRows = 8;                // a context's last tile is loaded in 8-row chunks
+constexpr int kChunkBytes = kChunkRows * 128;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -170,7 +173,9 @@ template <int GC>
 // 9-warp CTAs (5 warps on some sub-partitions) fit only at <= 102 registers per thread.
 __global__ void __maxnreg__(96)
     decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
-                        const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
+                        const __grid_constant__ CUtensorMap vmap,
+                        const __grid_constant__ CUtensorMap kmap8,
+                        const __grid_constant__ CUtensorMap vmap8, const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
   DecodeSmem<GC> &sm = *reinterpret_cast<DecodeSmem<GC> *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -205,6 +210,8 @@ __global__ void __maxnreg__(96)
   if (threadIdx.x == kConsumerWarps * 32) {
     prefetch_tensormap(&kmap);
     prefetch_tensormap(&vmap);
+    prefetch_tensormap(&kmap8);
+    prefetch_tensormap(&vmap8);
   }
   // the first tile's pool row as read ahead of the wait (-1: none), and its KV head
   int32_t spec_blk = -1, spec_row = -1, spec_h = 0;
@@ -259,6 +266,7 @@ __global__ void __maxnreg__(96)
     // a zeroed counter a CTA's first draw is below units + grid: anything else (or a draw
     // below zero) means the workspace's counter was not zero on entry.
     bool first_draw = true, past_end = false;
+    int last_rows = kTile;  // keys in the current unit's last tile
     auto draw = [&]() -> int {
       const int u = atomicAdd(p.queue, 1);
       if (first_draw) {
@@ -330,6 +338,7 @@ __global__ void __maxnreg__(96)
           // unit per KV head reads it: the launcher takes this path with one head group)
           un = Unit{b, s, xg, (int)((end - begin + kTile - 1) / kTile),
                     p.k_new != nullptr && end == L ? 1 : 0, 0};
+          last_rows = (int)(end - begin - (int64_t)(un.ntiles - 1) * kTile);
           if (spec_pending) {
             if (first_blk == spec_blk) first_it = 1;
             else un.skip = 1;
@@ -413,9 +422,26 @@ __global__ void __maxnreg__(96)
         } else {
           row = (int32_t)(blk * p.block_size + pos % p.block_size);
         }
-        mbar_arrive_expect_tx(&sm.full[stage], 2 * kTileBytes);
-        tma_load_3d(sm.k[stage], &kmap, &sm.full[stage], 0, row, 2 * h, policy);
-        tma_load_3d(sm.v[stage], &vmap, &sm.full[stage], 0, row, 2 * h, policy);
+        const int rows_here = it == un.ntiles - 1 ? last_rows : kTile;
+        if (rows_here >= kTile || row < 0) {
+          mbar_arrive_expect_tx(&sm.full[stage], 2 * kTileBytes);
+          tma_load_3d(sm.k[stage], &kmap, &sm.full[stage], 0, row, 2 * h, policy);
+          tma_load_3d(sm.v[stage], &vmap, &sm.full[stage], 0, row, 2 * h, policy);
+        } else {
+          // the unit's last tile ends inside the tile: only its 8-row chunks that hold keys
+          // (the consumers mask the rows past the context, whatever shared memory holds)
+          const int chunks = (rows_here + kChunkRows - 1) / kChunkRows;
+          mbar_arrive_expect_tx(&sm.full[stage], (uint32_t)(chunks * 4 * kChunkBytes));
+          for (int c = 0; c < chunks; ++c)
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+              const int off = hf * kPlaneBytes + c * kChunkBytes;
+              tma_load_3d(sm.k[stage] + off, &kmap8, &sm.full[stage], 0, row + kChunkRows * c,
+                          2 * h + hf, policy);
+              tma_load_3d(sm.v[stage] + off, &vmap8, &sm.full[stage], 0, row + kChunkRows * c,
+                          2 * h + hf, policy);
+            }
+        }
 
       }
     }
@@ -730,8 +756,9 @@ __global__ void __launch_bounds__(128)
 }
 
 template <int GC>
-cudaError_t launch_split(const CUtensorMap &km, const CUtensorMap &vm, const DecodeParams &prm,
-                         int num_sms, cudaStream_t stream) {
+cudaError_t launch_split(const CUtensorMap &km, const CUtensorMap &vm, const CUtensorMap &km8,
+                         const CUtensorMap &vm8, const DecodeParams &prm, int num_sms,
+                         cudaStream_t stream) {
   const size_t smem = smem_bytes<GC>(prm.cluster);
   static bool configured[64] = {};
   int dev = 0;
@@ -768,7 +795,7 @@ cudaError_t launch_split(const CUtensorMap &km, const CUtensorMap &vm, const Dec
     attr[1].val.clusterDim.z = 1;
     cfg.numAttrs = 2;
   }
-  return cudaLaunchKernelEx(&cfg, decode_split_kernel<GC>, km, vm, prm);
+  return cudaLaunchKernelEx(&cfg, decode_split_kernel<GC>, km, vm, km8, vm8, prm);
 }
 
 }  // namespace
@@ -816,17 +843,25 @@ DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
 cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &p, cudaStream_t stream) {
   // TMA views of the two pools: {64 dims, num_blocks * block_size rows, 2 * Hkv half-heads}
   // (the half-head stride, 128 bytes, is the innermost of the two): a tile lands as two
-  // planes, one per half of the head dimension
-  CUtensorMap km, vm;
+  // planes, one per half of the head dimension. The second pair of views moves 8 rows of one
+  // half: a context's last tile is loaded only as far as it holds keys.
+  CUtensorMap km, vm, km8, vm8;
   const uint64_t rows = (uint64_t)a.num_blocks * a.block_size;
   const uint64_t dims[3] = {64, rows, (uint64_t)a.num_kv_heads * 2};
   const uint64_t strides[2] = {(uint64_t)a.num_kv_heads * kD * 2, 128};
   const uint32_t box[3] = {64, kTile, 2};
+  const uint32_t box8[3] = {64, kChunkRows, 1};
   if (encode_tensor_map(&km, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(a.k_cache),
                         dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B) != CUDA_SUCCESS ||
       encode_tensor_map(&vm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(a.v_cache),
                         dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B) != CUDA_SUCCESS ||
+      encode_tensor_map(&km8, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(a.k_cache),
+                        dims, strides, box8, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B) != CUDA_SUCCESS ||
+      encode_tensor_map(&vm8, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(a.v_cache),
+                        dims, strides, box8, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
 
@@ -888,8 +923,8 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &p, cudaSt
   if (!queued) prm.queue = nullptr;
   if (e != cudaSuccess) return e;
   prm.cluster = !queued && p.splits >= 2 && p.splits <= kMaxCluster ? p.splits : 0;
-  e = p.heads_per_cta == 2 ? launch_split<2>(km, vm, prm, a.num_sms, stream)
-                           : launch_split<1>(km, vm, prm, a.num_sms, stream);
+  e = p.heads_per_cta == 2 ? launch_split<2>(km, vm, km8, vm8, prm, a.num_sms, stream)
+                           : launch_split<1>(km, vm, km8, vm8, prm, a.num_sms, stream);
   if (e != cudaSuccess || p.splits == 1 || prm.cluster) return e;
   const int64_t rows_out = (int64_t)a.batch * a.num_q_heads;
   // programmatic dependent launch: the merge grid is set up while the split kernel runs
