@@ -889,7 +889,8 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &p, cudaSt
   prm.chunk = p.chunk;
   prm.splits = p.splits;
   const int64_t units = (int64_t)p.splits * a.batch * prm.xgroups;
-  if (units > INT32_MAX) return cudaErrorInvalidValue;
+  // the work counter runs to units + grid size - 1 (an int): keep that in range
+  if (units + 2 * (int64_t)a.num_sms > INT32_MAX) return cudaErrorInvalidValue;
   prm.units = (int32_t)units;
   prm.qscale = a.scale * kLog2e;
   prm.num_kv_heads = a.num_kv_heads;
