@@ -196,6 +196,23 @@ def test_decode_workspace_too_small_is_rejected():
     assert e.value.status == pkv.ERR_WORKSPACE
 
 
+@pytest.mark.parametrize("n_seqs", [16, 64])
+def test_decode_last_tile_every_remainder(n_seqs):
+    """A context's last tile is loaded only as far as it holds keys (8-row chunks), so the
+    rest of that shared-memory stage keeps whatever an earlier tile left there -- often NaN
+    canaries from pool slots past other contexts. Contexts with every remainder 1..64 modulo
+    the 64-token tile, on a static grid whose splits merge in clusters (16 sequences) and on
+    the work queue (64 sequences: 512 units), must match the oracle."""
+    g = w.rng(75)
+    ctx = [64 * int(g.integers(0, 11)) + 1 + (i % 64) for i in range(n_seqs)]
+    lay, val = _host_case(ctx, seed=76)
+    ref = _oracle_step(lay, val)
+    out = _gpu_step(lay, dev(val.k_cache), dev(val.v_cache), dev(val.q), dev(val.k_new),
+                    dev(val.v_new), 0)
+    assert_attention_close(out, ref, f"every last-tile remainder, {n_seqs} sequences")
+    assert pkv.get_device_errors() == 0
+
+
 def test_decode_workspace_counter_left_zero_and_dirty_counter_flagged():
     """With more units than two per SM the CTAs take units from the work counter at the
     start of the workspace, and the CTA that draws last sets it back to zero: calls in a row
