@@ -160,12 +160,18 @@ def decode_workspace_bytes(batch: int, num_q_heads: int, num_kv_heads: int, head
 
 
 def decode_workspace(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
-                     max_context_len: int, num_splits: int = 0, device=None) -> torch.Tensor:
-    """A decode workspace, zeroed: its first 16 bytes are work counters that must be zero
-    before the first call (every call leaves them zero again)."""
+                     max_context_len: int, num_splits: int = 0, device=None,
+                     stream=None) -> torch.Tensor:
+    """A decode workspace, zeroed on `stream` (the current stream when None): its first word
+    is the split kernel's work counter, which must be zero before the first call (every call
+    leaves it at zero again). Calls on another stream must come after the zeroing."""
     n = decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, max_context_len,
                                num_splits)
-    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+    if stream is None:
+        return torch.zeros(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+    s = stream if isinstance(stream, torch.cuda.Stream) else torch.cuda.ExternalStream(int(stream))
+    with torch.cuda.stream(s):
+        return torch.zeros(max(n, 16), dtype=torch.uint8, device=device or "cuda")
 
 
 def paged_decode_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
@@ -187,7 +193,8 @@ def paged_decode_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
     if out is None:
         out = torch.empty_like(q)
     if workspace is None:
-        workspace = decode_workspace(B, hq, hkv, d, max_context_len, num_splits, q.device)
+        workspace = decode_workspace(B, hq, hkv, d, max_context_len, num_splits, q.device,
+                                     stream)
     _check("pkv_paged_decode_attn", _LIB.pkv_paged_decode_attn(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
         _ptr(context_lens), B, int(max_context_len), hq, hkv, d, bs, nb, float(scale),
@@ -222,7 +229,8 @@ def paged_decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
     if out is None:
         out = torch.empty_like(q)
     if workspace is None:
-        workspace = decode_workspace(B, hq, hkv, d, max_context_len, num_splits, q.device)
+        workspace = decode_workspace(B, hq, hkv, d, max_context_len, num_splits, q.device,
+                                     stream)
     _check("pkv_paged_decode_step", _LIB.pkv_paged_decode_step(
         _ptr(q), _ptr(k_new), k_new.stride(0), _ptr(v_new), v_new.stride(0), _ptr(slot_mapping),
         _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],

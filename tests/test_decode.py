@@ -287,6 +287,28 @@ def test_decode_batch_sweep(batch):
     _full_size(lay, 3000 + batch, check_rows=np.sort(rows))
 
 
+def test_decode_on_a_given_stream_without_a_workspace():
+    """A call given a stream and no workspace zeroes the workspace it allocates on that
+    stream, where the kernel reads its work counter (a queued grid: 48 sequences x 8 KV heads),
+    also when the stream is passed as a raw handle."""
+    lay, val = _host_case([500 + 7 * i for i in range(48)], seed=77)
+    oracle.kv_store(val.k_new, val.v_new, lay.slot_mapping, val.k_cache, val.v_cache)
+    ref = oracle.paged_decode(val.q, val.k_cache, val.v_cache, lay.block_tables,
+                              lay.context_lens, lay.scale)
+    q, kc, vc = dev(val.q), dev(val.k_cache), dev(val.v_cache)
+    bt, cl = dev(lay.block_tables), dev(lay.context_lens)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    for handle in (s, s.cuda_stream):
+        out = torch.empty_like(q)
+        torch.cuda.synchronize()
+        pkv.paged_decode_attn(q, kc, vc, bt, cl, lay.max_context_len, lay.scale, out=out,
+                              stream=handle)
+        s.synchronize()
+        assert_attention_close(out, ref, f"stream given as {type(handle).__name__}")
+    assert pkv.get_device_errors() == 0
+
+
 def test_decode_runs_on_the_callers_current_stream():
     """With no stream given, the binding launches on torch's current stream: a side stream's
     handle is what it passes, and a call made under that stream sees the inputs written on it."""
